@@ -1,0 +1,528 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled MoE expert hot path on GB300; prints ONE JSON
+line on rank 0.
+
+A step is one moe_expert_forward over the Qwen3-30B-A3B-shaped expert layer
+(T=16384 tokens, H=2048, E=128 experts, top-8, I=768): routing, per-token
+NVFP4 quantization of x into the routed slots, the tcgen05 grouped GEMM with
+gate/up weights and the fused SwiGLU + FP32 rescale, per-token NVFP4 of h, the
+grouped GEMM with down weights, and the weighted combine.  value = the two
+GEMMs' algorithmic FLOPs / step time (TFLOP/s), summed over all ranks (each
+rank runs its own replica: weak scaling, no collective on the data path).
+The working set (~0.9 GB: weights, activations, workspace) is larger than the
+129 MB L2, so no flush is needed between steps.
+
+Also reported: per-stage times (CUDA events recorded by the library on the
+launching stream inside the timed region), a roofline for the dominant
+kernel, the standalone quantizers (MXFP8 row+col on 16384x2048, NVFP4
+per-token on 16384x2048, requant with Philox SR on 16384x2048 and 16384x768;
+L2 flushed between launches), an end-to-end number through the public API
+with pinned-host inputs/outputs copied inside the timed region, SM clocks
+sampled during the timed region, and the CPU oracle's throughput on a
+bounded sample.
+
+--impl reference times the CPU oracle instead (on the host cores, rank 0
+only) on a bounded per-step sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "NVFP4 grouped expert GEMM TFLOPS + quantize GB/s, % of GB300 roofline"
+WORKLOADS = {
+    "qwen3": dict(T=16384, H=2048, E=128, k=8, I=768, seed=3, w_seed_gu=31, w_seed_d=32,
+                  name="Qwen3-30B-A3B-shaped MoE expert layer (T=16384, H=2048, E=128, top-8, I=768)"),
+    "deepseek": dict(T=32768, H=7168, E=256, k=8, I=2048, seed=5, w_seed_gu=51, w_seed_d=52, zipf=1.1,
+                     four_six=True,
+                     name="DeepSeek-V3-shaped MoE expert layer (T=32768, H=7168, E=256, top-8, I=2048, 4/6)"),
+}
+KERNELS_PER_STEP = 9  # route x3, quantize-scatter, pad rows, GEMM1, quantize h, GEMM2, combine
+
+
+def gemm_flops(w):
+    R = w["T"] * w["k"]
+    return 2.0 * R * (2 * w["I"]) * w["H"], 2.0 * R * w["H"] * w["I"]
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p.update({k: m[k] for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p["source"] = "measured"
+    # FP4 dense tensor peak = bf16 peak x the nominal FP4/BF16 ratio (13.5 / 2.25)
+    p["fp4_tflops"] = p["bf16_tflops"] * 6.0
+    p["fp4_tflops_sustained"] = p["bf16_tflops_sustained"] * 6.0
+    return p
+
+
+# ----------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.idx)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(self.NAMES, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_expert_pass(O, x_bits, rows_tok, wgu_q, wd_q, four_six):
+    """The oracle on one expert's routed rows: per-token NVFP4 of x, GEMM1
+    (fp64 on exact dequantized operands), SwiGLU, bf16 h, per-token NVFP4
+    of h, GEMM2.  Returns the FLOPs done."""
+    xq = O.nvfp4_quantize_rows(x_bits[rows_tok], four_six=four_six)
+    gu, _ = O.gemm_nvfp4(*xq, *wgu_q, with_abs=False)
+    h = O.f64_to_bf16_array(O.swiglu(gu))
+    hq = O.nvfp4_quantize_rows(h, four_six=four_six)
+    O.gemm_nvfp4(*hq, *wd_q, with_abs=False)
+    n, I2, H = rows_tok.size, wgu_q[0].shape[0], x_bits.shape[1]
+    return 2.0 * n * I2 * H + 2.0 * n * H * (I2 // 2)
+
+
+def oracle_setup(w, experts, x_bits=None, ids=None):
+    """Inputs for the oracle legs: x and routing from the workload's seeds,
+    the sampled experts' weights drawn on the host with the same
+    distribution, quantized by the oracle (untimed)."""
+    import oracle as O
+    from block_scaled_precision_quantize_gb300 import synth
+    O.build()
+    T, H, I, E, k = w["T"], w["H"], w["I"], w["E"], w["k"]
+    if x_bits is None:
+        x_bits = synth.normal((T, H), seed=w["seed"])
+    if ids is None:
+        ids, _ = synth.topk_routing(T, E, k, seed=w["seed"], zipf_s=w.get("zipf"))
+    qs = {}
+    for e in experts:
+        gu = synth.normal((1, 2 * I, H), seed=w["w_seed_gu"], stream=1000 + e, std=0.02)
+        dn = synth.normal((1, H, I), seed=w["w_seed_d"], stream=1000 + e, std=0.02)
+        c, s, t = O.nvfp4_quantize_group(gu)
+        c2, s2, t2 = O.nvfp4_quantize_group(dn)
+        qs[e] = ((c[0], s[0], t[0]), (c2[0], s2[0], t2[0]))
+    tok_of = {e: np.nonzero((ids == e).any(axis=1))[0] for e in experts}
+    return O, x_bits, qs, tok_of
+
+
+def cpu_baseline(w, x_bits, ids, budget_s=12.0):
+    """The oracle, as it stands, on whole routed segments of experts 0, 1, ...
+    until about budget_s seconds of work; single thread."""
+    experts = [0, 1, 2]
+    O, x_bits, qs, tok_of = oracle_setup(w, experts, x_bits, ids)
+    flops, t0, used = 0.0, time.perf_counter(), []
+    for e in experts:
+        flops += oracle_expert_pass(O, x_bits, tok_of[e], *qs[e], w.get("four_six", False))
+        used.append(e)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    rows = int(sum(tok_of[e].size for e in used))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"experts {used} whole routed segments ({rows} rows) through NVFP4 quantize, GEMM1, "
+                      f"SwiGLU, h quantize, GEMM2 on one host thread ({dt:.1f} s, {flops / 1e9:.1f} GFLOP)"}
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the oracle on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    K, W = args.steps, args.warmup
+    budget = 90.0
+    rows_per_step = int(max(1, min(256, (budget / max(1, K + W) - 0.12) / 0.004)))
+    experts = list(range(min(w["E"], 8)))
+    O, x_bits, qs, tok_of = oracle_setup(w, experts)
+    four_six = w.get("four_six", False)
+
+    def step(i):
+        e = experts[i % len(experts)]
+        toks = tok_of[e][: rows_per_step]
+        return oracle_expert_pass(O, x_bits, toks, *qs[e], four_six)
+
+    for i in range(W):
+        step(i)
+    flops, t0 = 0.0, time.perf_counter()
+    for i in range(K):
+        flops += step(i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"per step: {rows_per_step} routed rows of one expert (rotating over experts {experts[0]}..{experts[-1]}) "
+              f"through NVFP4 quantize, GEMM1, SwiGLU, h quantize, GEMM2, one host thread")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w["name"], "T": w["T"], "H": w["H"], "E": w["E"], "topk": w["k"], "I": w["I"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+def time_calls(fn, iters, flush=None):
+    """Average duration of fn() (CUDA events on the current stream), with an
+    optional L2 flush before each call (outside the events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for i in range(iters):
+        if flush is not None:
+            flush()
+        evs[i][0].record()
+        fn()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    t = [a.elapsed_time(b) for a, b in evs]
+    return statistics.mean(t), statistics.median(t)
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_scaled_precision_quantize_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel_key, src_hash):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec or rec.get("source_hash") != src_hash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args, w, rank, world, local):
+    import torch
+
+    import block_scaled_precision_quantize_gb300 as bsq
+    from block_scaled_precision_quantize_gb300 import synth
+
+    bsq.build()
+    bsq.load()
+    dev = torch.device("cuda", local)
+    T, H, I, E, k = w["T"], w["H"], w["I"], w["E"], w["k"]
+    four_six = w.get("four_six", False)
+    P = peaks()
+
+    # inputs (synthetic, seeded): x and routing on the host, weights on the device
+    x_bits = synth.normal((T, H), seed=w["seed"])
+    ids, wts = synth.topk_routing(T, E, k, seed=w["seed"], zipf_s=w.get("zipf"))
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_host = torch.from_numpy(ids).pin_memory()
+    wts_host = torch.from_numpy(wts).pin_memory()
+    x = x_host.to(dev)
+    ids_d = ids_host.to(dev)
+    wts_d = wts_host.to(dev)
+    wgu_b = synth.device_normal_bf16((E, 2 * I, H), seed=w["w_seed_gu"], std=0.02, device=dev)
+    wgu = bsq.quantize_nvfp4_per_expert(wgu_b)
+    del wgu_b
+    wd_b = synth.device_normal_bf16((E, H, I), seed=w["w_seed_d"], std=0.02, device=dev)
+    wd = bsq.quantize_nvfp4_per_expert(wd_b)
+    del wd_b
+    ws = torch.empty(bsq.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def fwd():
+        bsq.moe_expert_forward(x, ids_d, wts_d, wgu, wd, I, four_six=four_six, workspace=ws, y=y, dev_status=status)
+
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        fwd()
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for row in stage_ev:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    clocks = Clocks(f"GPU-{uuid}" if uuid is not None else local)
+    clocks.start()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        bsq.set_stage_events(stage_ev[i])
+        fwd()
+    t_end.record()
+    bsq.set_stage_events(None)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end) / K, world)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    names = ["route", "quantize_scatter", "gemm1_swiglu", "quantize_h", "gemm2", "combine"]
+    stage_ms = {n: statistics.mean(stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for i in range(K))
+                for s, n in enumerate(names)}
+    f1, f2 = gemm_flops(w)
+    flops = f1 + f2
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    R = T * k
+    L = bsq.moe_workspace_layout(T, H, I, E, k)
+    offsets = torch.empty(E + 1, dtype=torch.int32)
+    offsets.copy_(ws[L.offsets:L.offsets + 4 * (E + 1)].view(torch.int32))
+    R_pad = int(offsets[-1])
+    stage_bytes = {
+        "quantize_scatter": T * H * 2 + R * (H // 2 + H // 16 + 4),
+        "quantize_h": R_pad * I * 2 + R_pad * (I // 2 + I // 16 + 4),
+        "combine": R * H * 2 + T * H * 2 + R * 8,
+    }
+    stages = {}
+    for n in names:
+        d = {"ms": stage_ms[n]}
+        if n == "gemm1_swiglu":
+            d.update(tflops=f1 / (stage_ms[n] * 1e-3) / 1e12)
+            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops_sustained"]
+        elif n == "gemm2":
+            d.update(tflops=f2 / (stage_ms[n] * 1e-3) / 1e12)
+            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops_sustained"]
+        elif n in stage_bytes:
+            d.update(gbs=stage_bytes[n] / (stage_ms[n] * 1e-3) / 1e9)
+            d["frac_of_hbm"] = d["gbs"] / P["hbm_gbs"]
+        stages[n] = d
+
+    # roofline of the dominant kernel
+    dom = max(names, key=lambda n: stage_ms[n])
+    gemm_hash = source_hash("gemm_fp4.cu", "common.cuh")
+    if dom in ("gemm1_swiglu", "gemm2"):
+        fl = f1 if dom == "gemm1_swiglu" else f2
+        ach = fl / (stage_ms[dom] * 1e-3) / 1e12
+        tr = traffic_record(f"k_gemm_fp4:{dom}:{args.workload}", gemm_hash)
+        roof = {"kernel": f"k_gemm_fp4 ({dom})", "bound": "tensor", "achieved": ach,
+                "peak": P["fp4_tflops_sustained"], "unit": "TFLOP/s", "frac": ach / P["fp4_tflops_sustained"],
+                "traffic": tr, "peak_source": f"{P['source']} bf16 sustained x 6 (nominal FP4/BF16 ratio)",
+                "frac_of_page_15pf": ach / 15000.0}
+    else:
+        ach = stage_bytes.get(dom, 0) / (stage_ms[dom] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / P["hbm_gbs"], "traffic": None, "peak_source": P["source"]}
+
+    # end to end through the public API, host buffers copied inside the timed region
+    y_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    Ke = max(3, min(K, 30))
+
+    def e2e_step():
+        x.copy_(x_host, non_blocking=True)
+        ids_d.copy_(ids_host, non_blocking=True)
+        wts_d.copy_(wts_host, non_blocking=True)
+        fwd()
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / Ke, world)
+    e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+           "h2d_bytes_per_step": T * H * 2 + ids.nbytes + wts.nbytes, "d2h_bytes_per_step": T * H * 2}
+
+    components = {} if args.no_components else quantizer_components(bsq, synth, dev, P)
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e2m1 block-scaled, fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": w["name"], "T": T, "H": H, "E": E, "topk": k, "I": I, "seed": w["seed"],
+                       "four_six": four_six, "routed_rows": R, "padded_rows": R_pad,
+                       "gemm_tflop_per_step": flops / 1e12,
+                       "l2": "working set ~1 GB > 129 MB L2; no flush between steps",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "stages": stages, "components": components, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * K, "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x_bits, ids)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def quantizer_components(bsq, synth, dev, P):
+    """The standalone bandwidth-bound kernels, L2 flushed between launches."""
+    import torch
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    out = {}
+    iters = 30
+    # MXFP8 row + column copies, 16384 x 2048, row std 10^U(-3,2)
+    xm = torch.from_numpy(synth.rows_log_uniform_std(16384, 2048, seed=2).view(np.int16)).to(dev).view(torch.bfloat16)
+    rc = torch.empty(16384, 2048, dtype=torch.uint8, device=dev)
+    rs = torch.empty(16384, 64, dtype=torch.uint8, device=dev)
+    cc = torch.empty(2048, 16384, dtype=torch.uint8, device=dev)
+    cs = torch.empty(2048, 512, dtype=torch.uint8, device=dev)
+    L = bsq.load()
+    st = torch.cuda.current_stream(dev).cuda_stream
+
+    def mx():
+        L.quantize_mxfp8_rowcol(xm.data_ptr(), 16384, 2048, 2048, rc.data_ptr(), rs.data_ptr(), cc.data_ptr(),
+                                cs.data_ptr(), 0, None, st)
+
+    mean, med = time_calls(mx, iters, flush)
+    b = 16384 * 2048 * 2 + 2 * (16384 * 2048 + 16384 * 64)
+    out["mxfp8_rowcol_16384x2048"] = {"us": mean * 1e3, "bytes": b, "gbs": b / (mean * 1e-3) / 1e9,
+                                      "frac_of_hbm": b / (mean * 1e-3) / 1e9 / P["hbm_gbs"]}
+    # NVFP4 per-token, 16384 x 2048 (swizzled SF)
+    xq = torch.from_numpy(synth.normal((16384, 2048), seed=3).view(np.int16)).to(dev).view(torch.bfloat16)
+    codes = torch.empty(16384, 1024, dtype=torch.uint8, device=dev)
+    sf = torch.empty(16384 * 128, dtype=torch.uint8, device=dev)
+    t = torch.empty(16384, dtype=torch.float32, device=dev)
+
+    def nv():
+        L.quantize_nvfp4_per_token(xq.data_ptr(), 16384, 2048, 2048, codes.data_ptr(), sf.data_ptr(), t.data_ptr(),
+                                   bsq.SF_SWIZZLED, None, st)
+
+    mean, med = time_calls(nv, iters, flush)
+    b = 16384 * 2048 * 2 + 16384 * (1024 + 128 + 4)
+    out["nvfp4_per_token_16384x2048"] = {"us": mean * 1e3, "bytes": b, "gbs": b / (mean * 1e-3) / 1e9,
+                                         "frac_of_hbm": b / (mean * 1e-3) / 1e9 / P["hbm_gbs"]}
+    # requant with Philox SR, both targets, 16384 x 2048 and 16384 x 768
+    for K in (2048, 768):
+        xr = synth.normal_with_outliers(16384, K, seed=7)
+        c, s, tt = bsq.quantize_nvfp4_per_token(torch.from_numpy(xr.view(np.int16)).to(dev).view(torch.bfloat16),
+                                                swizzled=True)
+        ws = torch.empty(bsq.requant_workspace_size(16384, K), dtype=torch.uint8, device=dev)
+        o = {"nv_codes": torch.empty(K, 8192, dtype=torch.uint8, device=dev),
+             "nv_sf": torch.empty(K * 1024, dtype=torch.uint8, device=dev),
+             "nv_scale": torch.empty(K, dtype=torch.float32, device=dev),
+             "mx_codes": torch.empty(K, 16384, dtype=torch.uint8, device=dev),
+             "mx_sf": torch.empty(((K + 127) // 128 * 128) * 512, dtype=torch.uint8, device=dev)}
+        for sr in (True, False):
+            def rq():
+                bsq.requant_transpose_sr(c, s, tt, stochastic=sr, seed=7, swizzled=True, workspace=ws, out=o)
+
+            mean, med = time_calls(rq, iters, flush)
+            b = (16384 * K // 2 + 16384 * K // 16 + 16384 * 4) + (K * 8192 + K * 1024 + K * 4) + (K * 16384 + K * 512)
+            out[f"requant_{'sr' if sr else 'rne'}_16384x{K}"] = {
+                "us": mean * 1e3, "bytes": b, "gbs": b / (mean * 1e-3) / 1e9,
+                "frac_of_hbm": b / (mean * 1e-3) / 1e9 / P["hbm_gbs"]}
+    del flush_buf
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-components", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+    else:
+        run_ours(args, w, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,247 @@
+// common.cuh -- device helpers shared by the block-scaled quantization kernels:
+// bf16 bit handling, E2M1 / E4M3 / E8M0 conversions, the swizzled scale-factor
+// layout, the Philox4x32-10 counter-based generator and device status words.
+//
+// Numerics: scale arithmetic uses the IEEE round-to-nearest intrinsics
+// (__fdiv_rn, __frcp_rn, __fmul_rn, __fadd_rn, __fsub_rn) so that no FMA
+// contraction or approximate division changes a bit; the library is built
+// without fast math and without flush-to-zero.  This is the pages' rule that
+// the FP4 quantizer must not use fast math ("LMSYS Drops Miles ...", section
+// "The bit-exact quantizer contract").
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <stdint.h>
+
+#include "../../include/bsq.h"
+
+#define BSQ_DEVICE __device__ __forceinline__
+
+namespace bsq {
+
+constexpr float kNvfp4ScaleDivisor = 2688.0f;  // 6 (E2M1 max) * 448 (E4M3 max)
+constexpr float kFltMax = 3.402823466e+38f;
+
+// ---------------------------------------------------------------- status
+BSQ_DEVICE void report(int32_t* dev_status, int32_t code)
+{
+    if (dev_status != nullptr) atomicCAS(dev_status, BSQ_DEV_OK, code);
+}
+
+// ---------------------------------------------------------------- bf16
+// bf16 bits -> binary32 (exact widening)
+BSQ_DEVICE float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+BSQ_DEVICE float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max |x| of the two bf16 values in a word, as a 16-bit magnitude pattern
+// (for finite values the bit pattern orders like the magnitude)
+BSQ_DEVICE uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
+BSQ_DEVICE uint32_t fold_halves(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
+BSQ_DEVICE float bf16mag_to_f32(uint32_t m16) { return __uint_as_float(m16 << 16); }
+
+// ---------------------------------------------------------------- E2M1
+// Eight binary32 values -> eight E2M1 codes packed in a word (element i in
+// nibble i), round to nearest even, saturating at 6 (cvt ... satfinite).
+BSQ_DEVICE uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5, float v6, float v7)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+    return r;
+}
+
+// E2M1 code (low nibble) -> binary32, from the format definition:
+// magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign.
+BSQ_DEVICE float e2m1_to_f32(uint32_t nib)
+{
+    uint32_t em = nib & 7u;
+    uint32_t bits = (em < 2u) ? (em ? 0x3F000000u : 0u) : ((((em >> 1) + 126u) << 23) | ((em & 1u) << 22));
+    return __uint_as_float(bits | ((nib & 8u) << 28));
+}
+
+// ---------------------------------------------------------------- E4M3
+// Four binary32 values -> four E4M3 bytes (element i in byte i), RNE satfinite.
+BSQ_DEVICE uint32_t e4m3x4(float v0, float v1, float v2, float v3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
+}
+BSQ_DEVICE uint32_t e4m3_rn(float v) { return e4m3x4(v, 0.f, 0.f, 0.f) & 0xFFu; }
+
+// E4M3 byte -> binary32, from the format definition (bias 7, subnormals
+// m * 2^-9).  The NaN codes are outside the contract.
+BSQ_DEVICE float e4m3_to_f32(uint32_t c)
+{
+    uint32_t s = (c & 0x80u) << 24, e = (c >> 3) & 15u, m = c & 7u;
+    float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+    return __uint_as_float(__float_as_uint(mag) | s);
+}
+
+// ---------------------------------------------------------------- SF layout
+// Offset of scale factor (row, col) in the swizzled tile layout (tiles of 128
+// rows x 4 columns, 512 bytes, tile-row major; inside a tile
+// (r%32)*16 + (r/32)*4 + c%4).  ncol_tiles = ceil(SF columns / 4).
+BSQ_DEVICE int64_t sf_swizzled(int64_t row, int64_t col, int64_t ncol_tiles)
+{
+    int64_t r = row & 127;
+    return ((row >> 7) * ncol_tiles + (col >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (col & 3);
+}
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32 with 10 rounds (Salmon et al., SC'11): per round the counter
+// words 0 and 2 are multiplied by the two round constants (32x32 -> 64), the
+// high halves are xored with the other words and the key; the key is bumped
+// by the two Weyl constants between rounds.
+BSQ_DEVICE uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t p0_lo = 0xD2511F53u * c.x, p0_hi = __umulhi(0xD2511F53u, c.x);
+        const uint32_t p2_lo = 0xCD9E8D57u * c.z, p2_hi = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(p2_hi ^ c.y ^ k0, p2_lo, p0_hi ^ c.w ^ k1, p0_lo);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Random bits for 8 consecutive elements 8g .. 8g+7 of a stream: element
+// 8g + i takes the 16-bit half (i & 1) of word (i >> 1).
+BSQ_DEVICE uint4 sr_block_bits(uint64_t seed, uint32_t stream, uint64_t g)
+{
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, 0u), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+}
+BSQ_DEVICE uint32_t sr_pick16(uint4 w, int i)
+{
+    uint32_t word = (i >> 1) == 0 ? w.x : (i >> 1) == 1 ? w.y : (i >> 1) == 2 ? w.z : w.w;
+    return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+// ---------------------------------------------------------------- SR encoders
+// Stochastic rounding with 16 random bits r: with lo <= |v| < hi the two
+// neighbouring grid points, round up iff r < 65536 * (|v| - lo) / (hi - lo)
+// (exact in binary32: grid spacings are powers of two); |v| >= max saturates.
+BSQ_DEVICE uint32_t e2m1_sr(float v, uint32_t r16)
+{
+    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
+    const float a = fabsf(v);
+    if (a >= 6.0f) return sign | 7u;
+    float lo, step;
+    uint32_t c;
+    if (a < 2.0f) {            // grid 0, .5, 1, 1.5 (spacing 0.5)
+        c = (uint32_t)__fmul_rn(a, 2.0f);      // floor(2a), exact for a < 2
+        lo = __fmul_rn((float)c, 0.5f);
+        step = 0.5f;
+    } else if (a < 4.0f) {     // 2, 3 (spacing 1)
+        const uint32_t i = (uint32_t)a;       // 2 or 3
+        c = i + 2u;                           // codes 4, 5
+        lo = (float)i;
+        step = 1.0f;
+    } else {                   // 4 .. 6 (spacing 2)
+        c = 6u;
+        lo = 4.0f;
+        step = 2.0f;
+    }
+    const float f = __fdiv_rn(__fsub_rn(a, lo), step);  // exact
+    if ((float)r16 < __fmul_rn(f, 65536.0f)) c += 1u;
+    return sign | c;
+}
+
+BSQ_DEVICE uint32_t e4m3_sr(float v, uint32_t r16)
+{
+    const uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
+    const float a = fabsf(v);
+    if (a >= 448.0f) return sign | 0x7Eu;
+    const uint32_t ab = __float_as_uint(a);
+    float lo, step;
+    uint32_t code;
+    if (a < 0.015625f) {       // subnormal range of E4M3: grid m * 2^-9
+        const uint32_t m = (uint32_t)__fmul_rn(a, 512.0f);   // floor, exact scaling
+        lo = __fmul_rn((float)m, 0.001953125f);
+        step = 0.001953125f;
+        code = m;
+    } else {                   // normal: keep 3 mantissa bits
+        const uint32_t e = ab >> 23;                 // biased fp32 exponent
+        lo = __uint_as_float(ab & 0xFFF00000u);
+        step = __uint_as_float((e - 3u) << 23);      // 2^(e-127-3)
+        code = ((e - 120u) << 3) | ((ab >> 20) & 7u);
+    }
+    const float f = __fdiv_rn(__fsub_rn(a, lo), step);
+    if ((float)r16 < __fmul_rn(f, 65536.0f)) code += 1u;   // carries into the exponent correctly
+    return sign | code;
+}
+
+// ---------------------------------------------------------------- NVFP4 block
+// Scale math of one 16-element block (see quantize_nvfp4_per_token):
+// s = E4M3(rn(amax_b / rn(mult * t))), d = rn(decode(s) * t),
+// enc = d == 0 ? 0 : rn(1 / d) (infinite -> FLT_MAX).
+struct BlockScale {
+    uint32_t sf;
+    float d;
+    float enc;
+};
+BSQ_DEVICE BlockScale nvfp4_block_scale(float amax_b, float mult_t, float t)
+{
+    BlockScale b;
+    b.sf = e4m3_rn(__fdiv_rn(amax_b, mult_t));
+    b.d = __fmul_rn(e4m3_to_f32(b.sf), t);
+    float enc = (b.d == 0.0f) ? 0.0f : __frcp_rn(b.d);
+    b.enc = isinf(enc) ? kFltMax : enc;
+    return b;
+}
+
+// Squared error of a candidate block (codes packed 8 per word), summed by the
+// fixed tree p_j = s_j + s_{j+8}, q_j = p_j + p_{j+4}, r_j = q_j + q_{j+2}.
+BSQ_DEVICE float block_sse(const float x[16], uint32_t c_lo, uint32_t c_hi, float d)
+{
+    float sq[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t nib = ((i < 8 ? c_lo : c_hi) >> (4 * (i & 7))) & 0xFu;
+        const float e = __fsub_rn(x[i], __fmul_rn(e2m1_to_f32(nib), d));
+        sq[i] = __fmul_rn(e, e);
+    }
+    float p[8], q[4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) p[j] = __fadd_rn(sq[j], sq[j + 8]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = __fadd_rn(p[j], p[j + 4]);
+    return __fadd_rn(__fadd_rn(q[0], q[2]), __fadd_rn(q[1], q[3]));
+}
+
+// Quantize 16 values with a block scale; returns the two code words.
+BSQ_DEVICE uint2 encode16(const float x[16], float enc)
+{
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(x[i], enc);
+    return make_uint2(e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]),
+                      e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]));
+}
+
+// MXFP8 shared exponent from the bit pattern of a block maximum (> 0):
+// X = clamp(floor(log2 amax) - 8, -127, 127); returns X.
+BSQ_DEVICE int mx_exponent(uint32_t amax_bits)
+{
+    const int e = (int)(amax_bits >> 23);
+    return e == 0 ? -127 : max(e - 127 - 8, -127);
+}
+BSQ_DEVICE float mx_multiplier(int X) { return __uint_as_float((uint32_t)(127 - X) << 23); }  // 2^-X
+
+}  // namespace bsq

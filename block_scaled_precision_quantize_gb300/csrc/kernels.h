@@ -1,0 +1,57 @@
+// kernels.h -- launchers of the device kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bsq {
+
+void launch_nvfp4_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* sf,
+                       float* row_scale, const float* group_amax, int64_t rows_per_group, bool four_six, bool swz,
+                       int sms, cudaStream_t st);
+void launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t rows_per_group, float* group_amax,
+                       int sms, cudaStream_t st);
+void launch_group_finalize(float* scale, int64_t groups, cudaStream_t st);
+void launch_mxfp8_rowcol(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint8_t* rc, uint8_t* rs,
+                         uint8_t* cc, uint8_t* cs, bool swz, cudaStream_t st);
+void launch_sf_pad_zero(uint8_t* sf, int64_t rows, int64_t cols, int sms, cudaStream_t st);
+void launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
+                    unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
+                    uint64_t seed, bool sr, bool swz, cudaStream_t st);
+void launch_sf_swizzle(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, int dir, int sms,
+                       cudaStream_t st);
+void launch_format_probe(int kind, const float* in, const uint32_t* rbits, void* out, int64_t n, int sms,
+                         cudaStream_t st);
+void launch_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t n, uint16_t* out, int sms,
+                          cudaStream_t st);
+
+struct GemmArgs {
+    const uint8_t* a_codes;
+    const uint8_t* a_sf;
+    const float* a_scale;
+    const int32_t* offsets;
+    int64_t experts;
+    int64_t m_capacity;
+    int64_t K;
+    int64_t N;
+    const uint8_t* b_codes;
+    const uint8_t* b_sf;
+    const float* b_scale;
+    int32_t epilogue;
+    void* out;
+    int64_t ldo;
+    int32_t* dev_status;
+};
+cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st);
+
+void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_t* hist, int32_t* counts,
+                  int32_t* offsets, int32_t* slot_of, int32_t* row_src, int64_t capacity, int32_t* dev_status,
+                  cudaStream_t st);
+void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of,
+                          uint8_t* codes, uint8_t* sf, float* scale, bool four_six, int sms, cudaStream_t st);
+void launch_pad_rows(const int32_t* row_src, const int32_t* offsets, int32_t E, int64_t H, uint8_t* sf, float* scale,
+                     int sms, cudaStream_t st);
+void launch_combine(const uint16_t* out, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of, const float* w,
+                    uint16_t* y, int sms, cudaStream_t st);
+
+}  // namespace bsq

@@ -1,0 +1,280 @@
+// moe.cu -- the non-GEMM steps of the MoE expert forward: routing
+// (count / padded scan / stable slot assignment), per-token NVFP4
+// quantization scattered into the routed slots, and the weighted combine.
+//
+// Dispatch ("End-to-End 4-Bit Training" summary, section "第三个决定"): tokens
+// travel to their experts already quantized.  Each expert's rows form one
+// segment of the routed matrix, padded to a multiple of 128 rows (the GEMM
+// tile height); inside a segment rows are in ascending (token, k) order, so
+// the layout is deterministic.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsq {
+
+constexpr int RT_CHUNK = 4096;  // routed pairs per histogram chunk
+
+// Phase A: per-chunk expert histograms -> hist[chunk][E].
+__global__ void __launch_bounds__(256) k_route_hist(const int32_t* __restrict__ ids, int64_t n, int32_t E,
+                                                    int32_t* __restrict__ hist, int32_t* dev_status)
+{
+    extern __shared__ int32_t sh[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+    __syncthreads();
+    const int64_t i0 = (int64_t)blockIdx.x * RT_CHUNK, i1 = min(n, i0 + RT_CHUNK);
+    for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+        const int32_t e = __ldg(ids + i);
+        if (e >= 0 && e < E) atomicAdd(sh + e, 1);
+        else report(dev_status, BSQ_DEV_BAD_EXPERT);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = sh[e];
+}
+
+// Phase B (one CTA of 1024 threads): per expert, exclusive prefix of the chunk
+// histograms (in place) and the total; then the padded segment offsets.
+__global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ hist, int32_t nchunks, int32_t E,
+                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets)
+{
+    __shared__ int32_t part[1024];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 1024) {
+        const int e = e0 + threadIdx.x;
+        int32_t total = 0;
+        if (e < E) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int32_t v = hist[(int64_t)c * E + e];
+                hist[(int64_t)c * E + e] = total;
+                total += v;
+            }
+            counts[e] = total;
+        }
+        const int32_t padded = (e < E) ? ((total + 127) & ~127) : 0;
+        part[threadIdx.x] = padded;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+            const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+            __syncthreads();
+            part[threadIdx.x] += v;
+            __syncthreads();
+        }
+        if (e < E) offsets[e] = carry + part[threadIdx.x] - padded;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry += part[1023];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) offsets[E] = carry;
+}
+
+// Phase C: one warp per chunk walks its pairs in order, 32 at a time; lanes
+// routed to the same expert are ranked with __match_any_sync.
+__global__ void __launch_bounds__(32) k_route_assign(const int32_t* __restrict__ ids, int64_t n, int32_t E,
+                                                     const int32_t* __restrict__ hist,
+                                                     const int32_t* __restrict__ offsets,
+                                                     int32_t* __restrict__ slot_of, int32_t* __restrict__ row_src)
+{
+    extern __shared__ int32_t fill[];
+    const int lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32) fill[e] = offsets[e] + hist[(int64_t)blockIdx.x * E + e];
+    __syncwarp();
+    const int64_t i0 = (int64_t)blockIdx.x * RT_CHUNK, i1 = min(n, i0 + RT_CHUNK);
+    for (int64_t base = i0; base < i1; base += 32) {
+        const int64_t i = base + lane;
+        const bool valid = i < i1;
+        int32_t e = valid ? __ldg(ids + i) : -1;
+        if (e >= E) e = -1;
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        int32_t slot = -1;
+        if (valid && e >= 0) {
+            slot = fill[e] + rank;
+            row_src[slot] = (int32_t)i;
+        }
+        if (valid) slot_of[i] = slot;
+        __syncwarp();
+        if (e >= 0 && rank == 0) fill[e] += __popc(same);
+        __syncwarp();
+    }
+}
+
+// Per-token NVFP4 quantization of x, written to every routed slot of the
+// token (one warp per token, lane l owns 16-blocks l, l+32, ...).
+template <int BPL, bool FOUR_SIX>
+__global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, int64_t T, int64_t H,
+                                                       int32_t topk, const int32_t* __restrict__ slot_of,
+                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                       float* __restrict__ scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nblk = (int)(H >> 4);
+    const int64_t ncol_tiles = (nblk + 3) >> 2;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+        const uint16_t* xr = x + t * H;
+        uint4 va[BPL], vb[BPL];
+        uint32_t bmax[BPL];
+        uint32_t rmax = 0;
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            const int b = lane + 32 * i;
+            if (b < nblk) {
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(va[i].x), "=r"(va[i].y), "=r"(va[i].z), "=r"(va[i].w) : "l"(xr + 16 * b));
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(vb[i].x), "=r"(vb[i].y), "=r"(vb[i].z), "=r"(vb[i].w) : "l"(xr + 16 * b + 8));
+            } else {
+                va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            uint32_t m = 0;
+            const uint32_t w[8] = {va[i].x, va[i].y, va[i].z, va[i].w, vb[i].x, vb[i].y, vb[i].z, vb[i].w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = absmax_bf16x2(m, w[j]);
+            bmax[i] = fold_halves(m);
+            rmax = max(rmax, bmax[i]);
+        }
+        rmax = __reduce_max_sync(0xFFFFFFFFu, rmax);
+        const float tt = __fdiv_rn(bf16mag_to_f32(rmax), kNvfp4ScaleDivisor);
+        const float six_t = __fmul_rn(6.0f, tt), four_t = __fmul_rn(4.0f, tt);
+        int32_t slots[32];
+        int nslots = 0;
+        for (int j = 0; j < topk; ++j) {
+            const int32_t s = __ldg(slot_of + t * topk + j);
+            if (s >= 0) slots[nslots++] = s;
+        }
+        if (lane < nslots) scale[slots[lane]] = tt;
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            const int b = lane + 32 * i;
+            if (b >= nblk) continue;
+            uint2 c = make_uint2(0u, 0u);
+            uint32_t s = 0;
+            if (tt != 0.0f) {
+                float xs[16];
+                const uint32_t w[8] = {va[i].x, va[i].y, va[i].z, va[i].w, vb[i].x, vb[i].y, vb[i].z, vb[i].w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    xs[2 * j] = bf16_lo(w[j]);
+                    xs[2 * j + 1] = bf16_hi(w[j]);
+                }
+                const float ab = bf16mag_to_f32(bmax[i]);
+                const BlockScale s6 = nvfp4_block_scale(ab, six_t, tt);
+                c = encode16(xs, s6.enc);
+                s = s6.sf;
+                if (FOUR_SIX) {
+                    const BlockScale s4 = nvfp4_block_scale(ab, four_t, tt);
+                    const uint2 c4 = encode16(xs, s4.enc);
+                    if (block_sse(xs, c4.x, c4.y, s4.d) < block_sse(xs, c.x, c.y, s6.d)) {
+                        c = c4;
+                        s = s4.sf;
+                    }
+                }
+            }
+            for (int j = 0; j < nslots; ++j) {
+                const int64_t r = slots[j];
+                reinterpret_cast<uint2*>(codes + r * (H >> 1))[b] = c;
+                sf[sf_swizzled(r, b, ncol_tiles)] = (uint8_t)s;
+            }
+        }
+    }
+}
+
+// Padding rows of the routed matrix get zero scales (their products vanish).
+__global__ void k_pad_rows(const int32_t* __restrict__ row_src, const int32_t* __restrict__ offsets, int32_t E,
+                           int64_t H, uint8_t* __restrict__ sf, float* __restrict__ scale)
+{
+    const int64_t total = __ldg(offsets + E);
+    const int nblk = (int)(H >> 4);
+    const int64_t ncol_tiles = (nblk + 3) >> 2;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < total; r += nwarps) {
+        if (__ldg(row_src + r) >= 0) continue;
+        if (lane == 0) scale[r] = 0.0f;
+        for (int b = lane; b < (int)(ncol_tiles * 4); b += 32) sf[sf_swizzled(r, b, ncol_tiles)] = 0;
+    }
+}
+
+// Combine: y[t] = sum_j w[t][j] * out[slot_of[t*k + j]], binary32 in
+// ascending j, rounded to bf16.  One warp per token, 8 columns per lane step.
+__global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ out, int64_t T, int64_t H,
+                                                 int32_t topk, const int32_t* __restrict__ slot_of,
+                                                 const float* __restrict__ w, uint16_t* __restrict__ y)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+        for (int64_t c = 8 * lane; c < H; c += 256) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < topk; ++j) {
+                const int32_t s = __ldg(slot_of + t * topk + j);
+                if (s < 0) continue;
+                const float wj = __ldg(w + t * topk + j);
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(out + (int64_t)s * H + c));
+                const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wj, bf16_lo(q[i])));
+                    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wj, bf16_hi(q[i])));
+                }
+            }
+            uint4 o;
+            uint32_t* op = &o.x;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                op[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i])) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1])) << 16);
+            *reinterpret_cast<uint4*>(y + t * H + c) = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_t* hist, int32_t* counts,
+                  int32_t* offsets, int32_t* slot_of, int32_t* row_src, int64_t capacity, int32_t* dev_status,
+                  cudaStream_t st)
+{
+    const int64_t n = T * topk;
+    const int nchunks = (int)((n + RT_CHUNK - 1) / RT_CHUNK);
+    cudaMemsetAsync(row_src, 0xFF, (size_t)capacity * sizeof(int32_t), st);
+    if (nchunks > 0) k_route_hist<<<nchunks, 256, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, dev_status);
+    k_route_scan<<<1, 1024, 0, st>>>(hist, nchunks, E, counts, offsets);
+    if (nchunks > 0)
+        k_route_assign<<<nchunks, 32, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, offsets, slot_of, row_src);
+}
+
+void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of,
+                          uint8_t* codes, uint8_t* sf, float* scale, bool four_six, int sms, cudaStream_t st)
+{
+    const int nblk = (int)(H >> 4);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 16));
+#define BSQ_QS(B)                                                                                                  \
+    do {                                                                                                           \
+        if (four_six) k_quant_scatter<B, true><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);     \
+        else k_quant_scatter<B, false><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);            \
+    } while (0)
+    if (nblk <= 32) BSQ_QS(1);
+    else if (nblk <= 64) BSQ_QS(2);
+    else if (nblk <= 128) BSQ_QS(4);
+    else if (nblk <= 256) BSQ_QS(8);
+    else BSQ_QS(16);
+#undef BSQ_QS
+}
+
+void launch_pad_rows(const int32_t* row_src, const int32_t* offsets, int32_t E, int64_t H, uint8_t* sf, float* scale,
+                     int sms, cudaStream_t st)
+{
+    k_pad_rows<<<sms * 8, 256, 0, st>>>(row_src, offsets, E, H, sf, scale);
+}
+
+void launch_combine(const uint16_t* out, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of, const float* w,
+                    uint16_t* y, int sms, cudaStream_t st)
+{
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 16));
+    k_combine<<<grid, 256, 0, st>>>(out, T, H, topk, slot_of, w, y);
+}
+
+}  // namespace bsq

@@ -79,6 +79,7 @@ def _declare(L):
         "bsqo_nvfp4_dequantize": (None, [_P, _P, _P, _I64, _I64, _P]),
         "bsqo_nvfp4_block_candidate": (None, [_P, ctypes.c_float, ctypes.c_float, _P, _P, _P]),
         "bsqo_sf_swizzled_offset": (_I64, [_I64, _I64, _I64]),
+        "bsqo_sf_swizzle": (None, [_P, _I64, _I64, _P]),
         "bsqo_mxfp8_quantize_rowcol": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
         "bsqo_requant_transpose": (None, [_P, _P, _P, _I64, _I64, _INT, _U64, _P, _P, _P, _P, _P]),
         "bsqo_gemm_nvfp4": (None, [_P, _P, _P, _I64, _I64, _P, _P, ctypes.c_float, _I64, _P, _P]),
@@ -87,6 +88,7 @@ def _declare(L):
         "bsqo_swiglu": (None, [_P, _I64, _I64, _P]),
         "bsqo_combine": (None, [_P, _I64, _P, _P, _I64, _I64, _P]),
         "bsqo_f64_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+        "bsqo_f64_to_bf16_array": (None, [_P, _I64, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -220,18 +222,12 @@ def sf_swizzled_offset(row: int, kblock: int, K: int) -> int:
 
 
 def sf_to_swizzled(sf_linear: np.ndarray) -> np.ndarray:
-    """Place a linear [rows, K/16] SF matrix into the tensor-core layout
-    (rows padded to 128, K to 64; padding bytes are 0)."""
+    """Place a linear SF matrix [rows, cols] into the tensor-core layout
+    (rows padded to 128, columns to 4; padding bytes are 0)."""
     sf_linear = _c(sf_linear, np.uint8)
-    rows, nkb = sf_linear.shape
-    K = nkb * 16
-    rpad = (rows + 127) // 128 * 128
-    kpad = (K + 63) // 64 * 64
-    out = np.zeros(rpad * kpad // 16, np.uint8)
-    L = lib()
-    for r in range(rows):
-        for b in range(nkb):
-            out[L.bsqo_sf_swizzled_offset(r, b, K)] = sf_linear[r, b]
+    rows, cols = sf_linear.shape
+    out = np.empty(((rows + 127) // 128 * 128) * ((cols + 3) // 4 * 4), np.uint8)
+    lib().bsqo_sf_swizzle(_ptr(sf_linear), rows, cols, _ptr(out))
     return out
 
 
@@ -346,6 +342,7 @@ def f64_to_bf16(v: float) -> int:
 
 
 def f64_to_bf16_array(v: np.ndarray) -> np.ndarray:
-    L = lib()
-    flat = np.asarray(v, np.float64).ravel()
-    return np.array([L.bsqo_f64_to_bf16(float(x)) for x in flat], np.uint16).reshape(np.shape(v))
+    flat = _c(v, np.float64).ravel()
+    out = np.empty(flat.size, np.uint16)
+    lib().bsqo_f64_to_bf16_array(_ptr(flat), flat.size, _ptr(out))
+    return out.reshape(np.shape(v))

@@ -383,6 +383,16 @@ EXPORT int64_t bsqo_sf_swizzled_offset(int64_t row, int64_t kblock, int64_t K)
     return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + (kblock % 4);
 }
 
+/* Whole SF matrix [rows][cols] (cols = SF per row) into the layout above;
+ * padding bytes are 0.  out holds ceil(rows/128)*128 * ceil(cols/4)*4 bytes. */
+EXPORT void bsqo_sf_swizzle(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* out)
+{
+    int64_t rpad = (rows + 127) / 128 * 128, cpad = (cols + 3) / 4 * 4;
+    memset(out, 0, (size_t)(rpad * cpad));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) out[bsqo_sf_swizzled_offset(r, c, 16 * cols)] = sf[r * cols + c];
+}
+
 /* ------------------------------------------------------------------------
  * MXFP8.  [LMSYS] "Recipe 1: End-to-end MXFP8": every 32 consecutive E4M3
  * values share one E8M0 scale, blocks are one-dimensional; TransformerEngine
@@ -644,6 +654,11 @@ EXPORT uint16_t bsqo_f64_to_bf16(double v)
     if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);  /* overflow to inf */
     float f = (float)r;                           /* exact: r has <= 8 significant bits */
     return (uint16_t)(sign | (f32_to_bits(f) >> 16));
+}
+
+EXPORT void bsqo_f64_to_bf16_array(const double* v, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = bsqo_f64_to_bf16(v[i]);
 }
 
 /* Combine: y[t] = bf16( sum_{j < k} w[t][j] * out[slot_of[t*k + j]] ), fp64,

@@ -54,6 +54,7 @@ void bsqo_nvfp4_block_candidate(const float* x16, float t, float mult,
 void bsqo_nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* t,
                            int64_t rows, int64_t K, float* out);
 int64_t bsqo_sf_swizzled_offset(int64_t row, int64_t kblock, int64_t K);
+void bsqo_sf_swizzle(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* out);
 
 /* MXFP8 quantization */
 void bsqo_mxfp8_quantize_rowcol(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
@@ -85,6 +86,7 @@ void bsqo_swiglu(const double* gate_up, int64_t rows, int64_t I, double* h);
 void bsqo_combine(const uint16_t* out_rows, int64_t H, const int32_t* slot_of,
                   const float* topk_w, int64_t T, int64_t k, uint16_t* y);
 uint16_t bsqo_f64_to_bf16(double v);
+void bsqo_f64_to_bf16_array(const double* v, int64_t n, uint16_t* out);
 
 #ifdef __cplusplus
 }

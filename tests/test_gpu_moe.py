@@ -1,0 +1,183 @@
+"""GPU: moe_expert_forward against the oracle, stage by stage.
+
+A last-bit binary32 difference in the SwiGLU output h can legitimately flip
+an NVFP4 code of h, so the forward is checked in stages: routing (exact),
+quantize-scatter of x (bit-exact), GEMM1 + SwiGLU (GEMM tolerance + bf16),
+quantization of the GPU's own h (bit-exact), GEMM2 from the GPU's own
+quantized h (GEMM tolerance + bf16), combine of the GPU's own expert outputs
+(fp32 accumulation + bf16 rounding)."""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_quantize_gb300 import synth
+from conftest import bits_equal, first_mismatch, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _ws(ws, L, field, dtype, shape):
+    off = getattr(L, field)
+    n = int(np.prod(shape)) * np.dtype(dtype).itemsize
+    return to_np(ws[off:off + n]).view(dtype).reshape(shape)
+
+
+def _unswz(O, sf_swz, rows, cols):
+    """Inverse of the oracle's swizzle, via its offset function."""
+    out = np.empty((rows, cols), np.uint8)
+    r = np.arange(rows)[:, None]
+    c = np.arange(cols)[None, :]
+    ctiles = (cols + 3) // 4
+    off = ((r // 128) * ctiles + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+    out[:, :] = sf_swz[off]
+    # the offset formula above must agree with the oracle's layout function
+    assert O.sf_swizzled_offset(rows - 1, cols - 1, 16 * cols) == off[-1, -1]
+    return out
+
+
+def _bf16_bound(ref, ab, extra_rel=2.0 ** -8):
+    return 1e-4 * ab + extra_rel * np.abs(ref) + 1e-30
+
+
+class _ExpertQuant:
+    """Oracle quantization of one expert's weights at a time (cached), checked
+    bit-exact against the GPU per-expert quantizer's output for that expert."""
+
+    def __init__(self, O, w_bits, gpu_q):
+        self.O, self.w, self.g, self.cache, self.sf = O, w_bits, gpu_q, {}, None
+
+    def __getitem__(self, e):
+        if e not in self.cache:
+            c, s, t = self.O.nvfp4_quantize_group(self.w[e:e + 1])
+            N = self.w.shape[1]
+            assert bits_equal(to_np(self.g[0][e]), c[0]) and bits_equal(to_np(self.g[2][e:e + 1]), t)
+            if self.sf is None:
+                self.sf = _unswz(self.O, to_np(self.g[1]), self.w.shape[0] * N, self.w.shape[2] // 16)
+            assert bits_equal(self.sf[e * N:(e + 1) * N], s[0])
+            self.cache[e] = (c[0], s[0], t[0])
+        return self.cache[e]
+
+
+def _staged(gpu, O, T, H, I, E, k, four_six, seed, sample_rows=None):
+    x = synth.normal((T, H), seed=seed)
+    ids, wts = synth.topk_routing(T, E, k, seed=seed)
+    wgu_b = synth.normal((E, 2 * I, H), seed=seed + 1, std=0.02)
+    wd_b = synth.normal((E, H, I), seed=seed + 2, std=0.02)
+    wgu = gpu.quantize_nvfp4_per_expert(to_dev(wgu_b))
+    wd = gpu.quantize_nvfp4_per_expert(to_dev(wd_b))
+    # weights: oracle quantization per expert, bit-exact with the GPU's
+    GU = _ExpertQuant(O, wgu_b, wgu)
+    DN = _ExpertQuant(O, wd_b, wd)
+
+    L = gpu.moe_workspace_layout(T, H, I, E, k)
+    ws = torch.zeros(L.total, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, four_six=four_six,
+                               workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    cap = L.capacity
+
+    # 1. routing
+    offsets, slot_of, row_src = O.route(ids, E)
+    R = int(offsets[-1])
+    assert bits_equal(_ws(ws, L, "offsets", np.int32, (E + 1,)), offsets)
+    assert bits_equal(_ws(ws, L, "slot_of", np.int32, (T * k,)), slot_of)
+    assert bits_equal(_ws(ws, L, "row_src", np.int32, (cap,))[:R], row_src)
+
+    # 2. quantize-scatter of x (per-token scales, 4/6 as requested)
+    xc, xs, xt = O.nvfp4_quantize_rows(x, four_six=four_six)
+    src_tok = np.where(row_src >= 0, row_src // k, -1)
+    valid = src_tok >= 0
+    q_codes = _ws(ws, L, "xq_codes", np.uint8, (cap, H // 2))[:R]
+    q_scale = _ws(ws, L, "xq_scale", np.float32, (cap,))[:R]
+    q_sf = _unswz(O, _ws(ws, L, "xq_sf", np.uint8, (cap * (H // 16),)), cap, H // 16)[:R]
+    assert bits_equal(q_codes[valid], xc[src_tok[valid]]), first_mismatch(q_codes[valid], xc[src_tok[valid]])
+    assert bits_equal(q_sf[valid], xs[src_tok[valid]])
+    assert bits_equal(q_scale[valid], xt[src_tok[valid]])
+    assert not q_sf[~valid].any() and not q_scale[~valid].any()
+
+    rows = np.arange(R) if sample_rows is None else sample_rows(offsets, row_src)
+    expert_of = np.searchsorted(offsets, rows, side="right") - 1
+
+    # 3. GEMM1 + SwiGLU (on the oracle's own quantized x)
+    h_gpu = _ws(ws, L, "h", np.uint16, (cap, I))
+    ab = np.zeros((rows.size, 2 * I))
+    ref = np.zeros((rows.size, 2 * I))
+    for e in np.unique(expert_of):
+        sel = np.where(expert_of == e)[0]
+        rr = rows[sel]
+        tok = np.maximum(src_tok[rr], 0)
+        a_t = np.where(src_tok[rr] >= 0, xt[tok], 0).astype(np.float32)
+        o, a = O.gemm_nvfp4(xc[tok], xs[tok], a_t, *GU[e])
+        ref[sel], ab[sel] = o, a
+    h_ref = O.swiglu(ref)
+    g, u = ref[:, :I], ref[:, I:]
+    sg = g / (1 + np.exp(-g))
+    bound = 1.1 * np.abs(u) * 1e-4 * ab[:, :I] + np.abs(sg) * 1e-4 * ab[:, I:] + 2.0 ** -8 * np.abs(h_ref) + 1e-30
+    hg = synth.bf16_bits_to_f32(h_gpu[rows]).astype(np.float64)
+    assert np.all(np.abs(hg - h_ref) <= bound), np.max(np.abs(hg - h_ref) / bound)
+
+    # 4. quantization of the GPU's own h (bit-exact)
+    hc, hs, ht = O.nvfp4_quantize_rows(h_gpu[rows], four_six=four_six)
+    hq_codes = _ws(ws, L, "hq_codes", np.uint8, (cap, I // 2))
+    hq_scale = _ws(ws, L, "hq_scale", np.float32, (cap,))
+    hq_sf = _unswz(O, _ws(ws, L, "hq_sf", np.uint8, (cap * (I // 16),)), cap, I // 16)
+    assert bits_equal(hq_codes[rows], hc), first_mismatch(hq_codes[rows], hc)
+    assert bits_equal(hq_sf[rows], hs) and bits_equal(hq_scale[rows], ht)
+
+    # 5. GEMM2 from the GPU's own quantized h (bf16 expert outputs)
+    out_gpu = _ws(ws, L, "out", np.uint16, (cap, H))
+    for e in np.unique(expert_of):
+        sel = np.where(expert_of == e)[0]
+        rr = rows[sel]
+        o, a = O.gemm_nvfp4(hq_codes[rr], hq_sf[rr], hq_scale[rr], *DN[e])
+        got = synth.bf16_bits_to_f32(out_gpu[rr]).astype(np.float64)
+        assert np.all(np.abs(got - o) <= _bf16_bound(o, a)), e
+
+    # 6. combine of the GPU's own expert outputs
+    if sample_rows is None:
+        y_ref = O.combine(out_gpu, slot_of, wts)
+        yg = synth.bf16_bits_to_f32(to_np(y)).astype(np.float64)
+        yr = synth.bf16_bits_to_f32(y_ref).astype(np.float64)
+        of = synth.bf16_bits_to_f32(out_gpu).astype(np.float64)
+        terms = np.abs(of[slot_of.reshape(T, k)] * wts[:, :, None]).sum(axis=1)
+        assert np.all(np.abs(yg - yr) <= 2.0 ** -8 * np.abs(yr) + 1e-6 * terms + 1e-30)
+    return y
+
+
+@pytest.mark.parametrize("four_six", [False, True])
+def test_moe_staged_small(gpu, O, four_six):
+    _staged(gpu, O, T=200, H=256, I=128, E=5, k=3, four_six=four_six, seed=11)
+
+
+def test_moe_staged_skewed_routing(gpu, O):
+    _staged(gpu, O, T=300, H=512, I=256, E=9, k=8, four_six=False, seed=4)
+
+
+def test_moe_bad_expert_id_reported(gpu):
+    T, H, I, E, k = 64, 256, 128, 4, 2
+    x = synth.normal((T, H), seed=1)
+    ids, wts = synth.topk_routing(T, E, k, seed=1)
+    ids[5, 1] = 17
+    wgu = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, 2 * I, H), seed=2, std=0.02)))
+    wd = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, H, I), seed=3, std=0.02)))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gpu.DEV_BAD_EXPERT
+    assert torch.isfinite(y.float()).all()
+
+
+def test_moe_qwen3_shaped_sampled(gpu, O):
+    """The Qwen3-30B-A3B-shaped layer at full size (T=16384, H=2048, E=128,
+    top-8, I=768), checked stage by stage on sampled routed rows: the most
+    and least loaded experts and random rows."""
+    def sample(offsets, row_src):
+        g = np.random.default_rng(0)
+        counts = np.diff(offsets)
+        big, small = int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+        picks = [np.arange(offsets[big], offsets[big] + 48), np.arange(offsets[small], offsets[small] + 16),
+                 g.choice(int(offsets[-1]), 192, replace=False)]
+        return np.unique(np.concatenate(picks))
+    _staged(gpu, O, T=16384, H=2048, I=768, E=128, k=8, four_six=False, seed=3, sample_rows=sample)
