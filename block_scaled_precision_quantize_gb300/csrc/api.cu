@@ -158,8 +158,10 @@ bsq_status quantize_mxfp8_rowcol(const void* x, int64_t rows, int64_t K, int64_t
 
 size_t bsq_requant_workspace_size(int64_t rows, int64_t K, int32_t nvfp4_target)
 {
-    (void)rows;
-    return (nvfp4_target && K > 0) ? align256((size_t)K * sizeof(float)) : 0;
+    if (!nvfp4_target || K <= 0 || rows <= 0) return 0;
+    // column maxima [K] (padded to 64) + per-32-row-chunk maxima [ceil(rows/32)][K]
+    const size_t nchunks = (size_t)((rows + 31) / 32);
+    return align256(((size_t)((K + 63) & ~(int64_t)63) + nchunks * (size_t)K) * sizeof(float));
 }
 
 bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
@@ -233,6 +235,7 @@ bsq_status grouped_expert_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_sf, 
     g.out = out;
     g.ldo = ldo;
     g.dev_status = dev_status;
+    g.sms = sms;
     return launch_gemm_fp4(g, stream) == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
 }
 
@@ -328,6 +331,7 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
     g1.out = ws + L.h;
     g1.ldo = I;
     g1.dev_status = dev_status;
+    g1.sms = sms;
     if (launch_gemm_fp4(g1, stream) != cudaSuccess) return BSQ_ERR_CUDA;
     stage_mark(3, stream);
 

@@ -142,23 +142,23 @@ BSQ_DEVICE uint32_t e2m1_sr(float v, uint32_t r16)
     const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
     const float a = fabsf(v);
     if (a >= 6.0f) return sign | 7u;
-    float lo, step;
+    float lo, inv_step;  // the spacing is a power of two, so * (1/spacing) is exact
     uint32_t c;
     if (a < 2.0f) {            // grid 0, .5, 1, 1.5 (spacing 0.5)
         c = (uint32_t)__fmul_rn(a, 2.0f);      // floor(2a), exact for a < 2
         lo = __fmul_rn((float)c, 0.5f);
-        step = 0.5f;
+        inv_step = 2.0f;
     } else if (a < 4.0f) {     // 2, 3 (spacing 1)
         const uint32_t i = (uint32_t)a;       // 2 or 3
         c = i + 2u;                           // codes 4, 5
         lo = (float)i;
-        step = 1.0f;
+        inv_step = 1.0f;
     } else {                   // 4 .. 6 (spacing 2)
         c = 6u;
         lo = 4.0f;
-        step = 2.0f;
+        inv_step = 0.5f;
     }
-    const float f = __fdiv_rn(__fsub_rn(a, lo), step);  // exact
+    const float f = __fmul_rn(__fsub_rn(a, lo), inv_step);  // exact
     if ((float)r16 < __fmul_rn(f, 65536.0f)) c += 1u;
     return sign | c;
 }
@@ -169,20 +169,20 @@ BSQ_DEVICE uint32_t e4m3_sr(float v, uint32_t r16)
     const float a = fabsf(v);
     if (a >= 448.0f) return sign | 0x7Eu;
     const uint32_t ab = __float_as_uint(a);
-    float lo, step;
+    float lo, inv_step;  // 1 / grid spacing, an exact power of two
     uint32_t code;
     if (a < 0.015625f) {       // subnormal range of E4M3: grid m * 2^-9
         const uint32_t m = (uint32_t)__fmul_rn(a, 512.0f);   // floor, exact scaling
         lo = __fmul_rn((float)m, 0.001953125f);
-        step = 0.001953125f;
+        inv_step = 512.0f;
         code = m;
     } else {                   // normal: keep 3 mantissa bits
-        const uint32_t e = ab >> 23;                 // biased fp32 exponent
+        const uint32_t e = ab >> 23;                 // biased fp32 exponent (121..135)
         lo = __uint_as_float(ab & 0xFFF00000u);
-        step = __uint_as_float((e - 3u) << 23);      // 2^(e-127-3)
+        inv_step = __uint_as_float((257u - e) << 23); // 2^-(e-127-3)
         code = ((e - 120u) << 3) | ((ab >> 20) & 7u);
     }
-    const float f = __fdiv_rn(__fsub_rn(a, lo), step);
+    const float f = __fmul_rn(__fsub_rn(a, lo), inv_step);
     if ((float)r16 < __fmul_rn(f, 65536.0f)) code += 1u;   // carries into the exponent correctly
     return sign | code;
 }

@@ -9,20 +9,32 @@
 // belongs in the GEMM epilogue rather than in a separate pass (same page,
 // section "Results"); SwiGLU experts run gate and up as one fused matmul
 // ("Miles Blackwell RL ...", section "Un quantizzatore condiviso è il vero
-// meccanismo").
+// meccanismo"); on GB300 the FP4 tensor cores are fast enough that feeding
+// them is the hard part ("End-to-End 4-Bit Training", section "工程细节").
 //
-// CTA = one 128-row x 256-column output tile of one expert (the grouped
-// problem is flattened: 128-row tiles of the expert-sorted A, each inside one
-// expert's segment, times the N tiles).  Warp roles (192 threads):
-//   warp 0      TMA producer: A tile (128 x 256 fp4), B tile (2 x 128 rows),
-//               and the SF chunks (512-byte tensor-core tiles) per stage
-//   warp 1      allocates tensor memory; one lane copies SF into tensor memory
-//               (tcgen05.cp) and issues the MMAs (128 x 128 x 64 each)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads lanes
-//               32*(w%4)..+31), rescale, SwiGLU, stores
+// Persistent kernel, one CTA per SM.  The grouped problem is flattened into
+// 128-row x 256-column output tiles (128-row tiles of the expert-sorted A,
+// each inside one expert's segment, times the N tiles), walked round-robin.
+// On sm_103 a single thread issuing tcgen05 instructions needs ~100+ cycles
+// per instruction, about what one 128x256x64 FP4 MMA computes, so the design
+// keeps that thread's instruction stream down to the MMAs themselves:
+//   warp 0      TMA producer, 4 copies per 256-wide K stage: A (128 x 128 B),
+//               B (256 rows: one 2-D box, or gate + up blocks in one 4-D box
+//               for SwiGLU), A's SF (one 2 KB bulk copy) and B's SF (two
+//               512-byte-chunk runs in one 2-D/3-D box of u64 elements)
+//   warp 1      allocates tensor memory; one lane issues one
+//               128 x 256 x 64 MMA per K step and the commits
+//   warps 2-5   one per tensor-memory lane quadrant: copy each stage's scale
+//               factors from shared into tensor memory with tcgen05.st (the
+//               layout tcgen05.cp 32x128b.warpx4 would produce: every
+//               quadrant holds the 32 x 16-byte chunk rows), then signal
+//   warps 6-21  epilogue, four warps per lane quadrant, 64 columns each: load
+//               the accumulator, hand it back to the MMA warp at once, then
+//               rescale / SwiGLU / store while the next tile's MMAs run
 // Shared memory: GM_STAGES stages of [SFA 2 KB][SFB 4 KB][A 16 KB][B 32 KB]
-// (A and B 128-byte swizzled, 1024-byte aligned).  Tensor memory: 512 columns
-// = accumulator (256) + an SF ring (48 per stage).
+// (A and B 128-byte swizzled, 1024-byte aligned) and the expert offsets.
+// Tensor memory: 512 columns = accumulator (256) + an SF ring (48 per stage:
+// SFA k-step j at 4j, SFB k-step j at 16 + 8j, both N halves side by side).
 // Every mbarrier wait is bounded; on expiry the CTA records BSQ_DEV_TIMEOUT,
 // drains its outstanding copies and MMAs (bounded), frees tensor memory and
 // returns.
@@ -33,7 +45,9 @@
 
 namespace bsq {
 
-constexpr int GM_THREADS = 192;
+constexpr int GM_SF_WARPS = 4;
+constexpr int GM_EPI_WARPS = 16;
+constexpr int GM_THREADS = 32 * (2 + GM_SF_WARPS + GM_EPI_WARPS);  // 704
 constexpr int GM_STAGES = 4;
 constexpr int GM_SFA_OFF = 0;
 constexpr int GM_SFB_OFF = 2048;
@@ -43,13 +57,14 @@ constexpr int GM_STAGE_BYTES = 6144 + 16384 + 32768;  // 55296 = 54 KB
 constexpr int GM_TMEM_COLS = 512;
 constexpr int GM_SF_RING = 256;                       // first SF column
 constexpr int GM_SF_STAGE_COLS = 48;
+constexpr int GM_MAX_SMEM_EXPERTS = 1024;             // offsets cached in shared memory up to this E
 constexpr uint32_t GM_SPIN_LIMIT = 1u << 22;
-constexpr size_t GM_SMEM_BYTES = (size_t)GM_STAGES * GM_STAGE_BYTES + 1024 + 1024;
+constexpr size_t GM_SMEM_BYTES = (size_t)GM_STAGES * GM_STAGE_BYTES + 1024;
 
-// Instruction descriptor, kind::mxf4nvf4: A and B are E2M1 (format 1),
-// K-major, no negation, N = 128 (N>>3 at bit 17), M = 128 (M>>4 at bit 24),
-// scale type UE4M3 (bit 23 = 0), scale-factor ids 0, dense.
-constexpr uint32_t GM_IDESC = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// Instruction descriptors, kind::mxf4nvf4: A and B are E2M1 (format 1),
+// K-major, no negation, N>>3 at bit 17, M = 128 (M>>4 at bit 24), scale type
+// UE4M3 (bit 23 = 0), scale-factor ids 0, dense, K = 64.
+__host__ __device__ constexpr uint32_t gm_idesc(uint32_t n) { return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24); }
 
 // ------------------------------------------------------------------ PTX
 BSQ_DEVICE uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -133,6 +148,29 @@ BSQ_DEVICE void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t ides
         : "memory");
 }
 
+// 32 consecutive accumulator columns of this warp's 32 lanes, without waiting.
+BSQ_DEVICE void tc_ld32_issue(uint32_t taddr, uint32_t r[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+// Wait for this thread's outstanding tcgen05.ld, then make every loaded
+// register depend on the wait so no use can be scheduled before it.
+template <int N>
+BSQ_DEVICE void tc_ld_wait(uint32_t (&r)[N])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 BSQ_DEVICE void tc_ld32(uint32_t taddr, float v[32])
 {
     uint32_t r[32];
@@ -157,14 +195,51 @@ BSQ_DEVICE uint32_t pack_bf16x2(float lo, float hi)
     return l | (h << 16);
 }
 
-BSQ_DEVICE float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+BSQ_DEVICE void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+BSQ_DEVICE void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+BSQ_DEVICE void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+// Store 16 / 32 consecutive tensor-memory columns of this warp's 32 lanes.
+BSQ_DEVICE void tc_st16(uint32_t taddr, const uint32_t* r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// h = silu(g) * u with silu(g) = g / (1 + e^-g); approximate exponential and
+// division (relative error ~1e-6, far below the bf16 output rounding); the
+// e^-g -> inf limit gives h -> 0.
+BSQ_DEVICE float swiglu1(float g, float u) { return __fdividef(g * u, 1.0f + __expf(-g)); }
 
 // ------------------------------------------------------------------ kernel
 struct GemmParams {
     const uint8_t* a_sf;
     const float* a_scale;
     const int32_t* offsets;
-    const uint8_t* b_sf;
     const float* b_scale;
     void* out;
     int32_t* dev_status;
@@ -177,58 +252,43 @@ struct GemmParams {
     int32_t epilogue;
 };
 
+struct TileInfo {
+    int m0, nt, e, n_halves;
+};
+
 __global__ void __launch_bounds__(GM_THREADS, 1)
-    k_gemm_fp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p)
+    k_gemm_fp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmSFB, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[2 * GM_STAGES + 2];
+    __shared__ __align__(8) uint64_t bars[3 * GM_STAGES + 3];
+    __shared__ int32_t s_off[GM_MAX_SMEM_EXPERTS + 1];
     __shared__ uint32_t s_tmem_base;
-    __shared__ int s_abort;
+    __shared__ int s_abort, s_bad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = blockIdx.x % p.n_tiles;
-    const int m0 = (blockIdx.x / p.n_tiles) * 128;
-
-    // ---- which expert owns rows [m0, m0+128)?
     const int E = p.experts;
-    const int total = __ldg(p.offsets + E);
-    if (m0 >= total) return;  // beyond the routed rows: nothing to do (no barrier/TMEM touched yet)
-    int lo = 0, hi = E - 1;   // largest e with offsets[e] <= m0
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.offsets + mid) <= m0) lo = mid; else hi = mid - 1;
-    }
-    const int e = lo;
-    {
-        // segment starts are multiples of 128; the total (offsets[E]) need not be
-        const int seg0 = __ldg(p.offsets + e), seg1 = __ldg(p.offsets + e + 1);
-        if ((seg0 & 127) || (e + 1 < E && (seg1 & 127)) || seg1 < seg0 || total > p.m_capacity || total < 0) {
-            if (threadIdx.x == 0) report(p.dev_status, BSQ_DEV_BAD_OFFSETS);
-            return;
-        }
-    }
-
-    const bool swiglu = p.epilogue == BSQ_EPI_SWIGLU_BF16;
-    const int n_halves = swiglu ? 2 : ((nt * 256 + 128 < p.N) ? 2 : 1);
-    const int brow0 = swiglu ? e * p.N + nt * 128 : e * p.N + nt * 256;
-    const int brow1 = swiglu ? e * p.N + (p.N >> 1) + nt * 128 : brow0 + 128;
-    const int k64_total = p.K >> 6;
-    const int kt_count = (k64_total + 3) >> 2;
+    const bool off_in_smem = E <= GM_MAX_SMEM_EXPERTS;
+    for (int i = threadIdx.x; i <= E && off_in_smem; i += blockDim.x) s_off[i] = __ldg(p.offsets + i);
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(GM_STAGES + s); };
-    const uint32_t acc_bar = bar0 + 8u * (2 * GM_STAGES);
-    const uint32_t drain_bar = bar0 + 8u * (2 * GM_STAGES + 1);
+    auto sf_bar = [&](int s) { return bar0 + 8u * (uint32_t)(2 * GM_STAGES + s); };
+    const uint32_t acc_full = bar0 + 8u * (3 * GM_STAGES);
+    const uint32_t acc_empty = bar0 + 8u * (3 * GM_STAGES + 1);
+    const uint32_t drain_bar = bar0 + 8u * (3 * GM_STAGES + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < GM_STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+            mbar_init(sf_bar(s), GM_SF_WARPS);
         }
-        mbar_init(acc_bar, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, GM_EPI_WARPS);
         mbar_init(drain_bar, 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -246,143 +306,234 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     const uint32_t tmem = s_tmem_base;
     volatile int* abort_flag = &s_abort;
 
+    auto off = [&](int i) { return off_in_smem ? s_off[i] : __ldg(p.offsets + i); };
+    // Offsets contract: ascending, segment starts multiples of 128, total <= capacity.
+    if (threadIdx.x == 0) {
+        int bad = 0;
+        for (int i = 0; i < E && !bad; ++i) {
+            const int a = off(i), b = off(i + 1);
+            bad = (a & 127) || b < a;
+        }
+        const int total = off(E);
+        bad = bad || total > p.m_capacity || total < 0;
+        s_bad = bad;
+        if (bad) report(p.dev_status, BSQ_DEV_BAD_OFFSETS);
+    }
+    __syncthreads();
+
+    const bool swiglu = p.epilogue == BSQ_EPI_SWIGLU_BF16;
+    const int k64_total = p.K >> 6;
+    const int kt_count = (k64_total + 3) >> 2;
+    const int m_tiles = s_bad ? 0 : (off(E) + 127) >> 7;
+    const int total_tiles = m_tiles * p.n_tiles;
+
+    auto tile_info = [&](int tile) {
+        TileInfo t;
+        t.nt = tile % p.n_tiles;
+        t.m0 = (tile / p.n_tiles) * 128;
+        int lo = 0, hi = E - 1;  // largest e with offsets[e] <= m0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off(mid) <= t.m0) lo = mid; else hi = mid - 1;
+        }
+        t.e = lo;
+        t.n_halves = swiglu ? 2 : ((t.nt * 256 + 128 < p.N) ? 2 : 1);
+        return t;
+    };
+
     if (warp == 0) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
-            const uint8_t* sfa_src = p.a_sf + ((size_t)(m0 >> 7) * k64_total) * 512;
-            const uint8_t* sfb_src0 = p.b_sf + ((size_t)(brow0 >> 7) * k64_total) * 512;
-            const uint8_t* sfb_src1 = p.b_sf + ((size_t)(brow1 >> 7) * k64_total) * 512;
-            int issued = 0;
-            for (int kt = 0; kt < kt_count; ++kt) {
-                const int s = kt % GM_STAGES;
-                const uint32_t ph = (uint32_t)(kt / GM_STAGES) & 1u;
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
-                    *abort_flag = 1;
-                    report(p.dev_status, BSQ_DEV_TIMEOUT);
-                    break;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmSFB)) : "memory");
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+                const TileInfo t = tile_info(tile);
+                const uint8_t* sfa_src = p.a_sf + ((size_t)(t.m0 >> 7) * k64_total) * 512;
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = (int)(it % GM_STAGES);
+                    const uint32_t ph = (it / GM_STAGES) & 1u;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
+                        *abort_flag = 1;
+                        report(p.dev_status, BSQ_DEV_TIMEOUT);
+                        break;
+                    }
+                    const int nk = min(4, k64_total - 4 * kt);
+                    const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
+                    // boxes always deliver their full size (out-of-range parts are zero-filled)
+                    mbar_expect_tx(full_bar(s), 16384u + 32768u + 4096u + (uint32_t)nk * 512u);
+                    tma_load_2d(st + GM_A_OFF, &tmA, kt * 128, t.m0, full_bar(s));
+                    if (swiglu) {
+                        tma_load_4d(st + GM_B_OFF, &tmB, kt * 128, t.nt * 128, 0, t.e, full_bar(s));
+                        tma_load_3d(st + GM_SFB_OFF, &tmSFB, kt * 256, t.nt, 2 * t.e, full_bar(s));
+                    } else {
+                        tma_load_2d(st + GM_B_OFF, &tmB, kt * 128, t.e * p.N + t.nt * 256, full_bar(s));
+                        tma_load_2d(st + GM_SFB_OFF, &tmSFB, kt * 256, (t.e * p.N + t.nt * 256) >> 7, full_bar(s));
+                    }
+                    bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 2048, (uint32_t)nk * 512u, full_bar(s));
                 }
-                const int nk = min(4, k64_total - 4 * kt);
-                const uint32_t sf_bytes = (uint32_t)nk * 512u;
-                const uint32_t bytes = 16384u + 16384u * (uint32_t)n_halves + sf_bytes * (uint32_t)(1 + n_halves);
-                const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
-                mbar_expect_tx(full_bar(s), bytes);
-                tma_load_2d(st + GM_A_OFF, &tmA, kt * 128, m0, full_bar(s));
-                tma_load_2d(st + GM_B_OFF, &tmB, kt * 128, brow0, full_bar(s));
-                if (n_halves == 2) tma_load_2d(st + GM_B_OFF + 16384, &tmB, kt * 128, brow1, full_bar(s));
-                bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 2048, sf_bytes, full_bar(s));
-                bulk_load(st + GM_SFB_OFF, sfb_src0 + (size_t)kt * 2048, sf_bytes, full_bar(s));
-                if (n_halves == 2) bulk_load(st + GM_SFB_OFF + 2048, sfb_src1 + (size_t)kt * 2048, sf_bytes, full_bar(s));
-                ++issued;
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA exits
-                for (int kt = max(0, issued - GM_STAGES); kt < issued; ++kt) {
+                for (uint32_t j = (it > GM_STAGES ? it - GM_STAGES : 0u); j < it; ++j)
                     for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
-                        if (mbar_try_wait(full_bar(kt % GM_STAGES), (uint32_t)(kt / GM_STAGES) & 1u)) break;
-                }
+                        if (mbar_try_wait(full_bar((int)(j % GM_STAGES)), (j / GM_STAGES) & 1u)) break;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            uint32_t it = 0, tc = 0;
             bool issued_any = false;
-            for (int kt = 0; kt < kt_count; ++kt) {
-                const int s = kt % GM_STAGES;
-                const uint32_t ph = (uint32_t)(kt / GM_STAGES) & 1u;
-                if (!mbar_wait(full_bar(s), ph, abort_flag)) {
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++tc) {
+                const TileInfo t = tile_info(tile);
+                const uint32_t idesc = gm_idesc(t.n_halves == 2 ? 256u : 128u);
+                // the epilogue has taken the previous accumulator out of tensor memory
+                if (!mbar_wait(acc_empty, (tc & 1u) ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     report(p.dev_status, BSQ_DEV_TIMEOUT);
                     break;
                 }
                 tc_fence_after();
-                const int nk = min(4, k64_total - 4 * kt);
-                const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
-                const uint32_t sf_col = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS;
-                for (int j = 0; j < nk; ++j) {
-                    tc_cp_sf(sf_col + 4 * j, smem_desc(st + GM_SFA_OFF + 512 * j, 16, 128, 0));
-                    tc_cp_sf(sf_col + 16 + 4 * j, smem_desc(st + GM_SFB_OFF + 512 * j, 16, 128, 0));
-                    if (n_halves == 2)
-                        tc_cp_sf(sf_col + 32 + 4 * j, smem_desc(st + GM_SFB_OFF + 2048 + 512 * j, 16, 128, 0));
-                }
-                for (int j = 0; j < nk; ++j) {
-                    const uint64_t ad = smem_desc(st + GM_A_OFF + 32 * j, 16, 1024, 2);
-                    const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
-                    for (int h = 0; h < n_halves; ++h) {
-                        const uint64_t bd = smem_desc(st + GM_B_OFF + 16384 * h + 32 * j, 16, 1024, 2);
-                        tc_mma(tmem + 128 * h, ad, bd, GM_IDESC, sf_col + 4 * j, sf_col + 16 + 16 * h + 4 * j, acc);
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = (int)(it % GM_STAGES);
+                    const uint32_t ph = (it / GM_STAGES) & 1u;
+                    if (!mbar_wait(sf_bar(s), ph, abort_flag)) {  // implies the stage's data has landed
+                        *abort_flag = 1;
+                        report(p.dev_status, BSQ_DEV_TIMEOUT);
+                        break;
                     }
+                    tc_fence_after();
+                    const int nk = min(4, k64_total - 4 * kt);
+                    const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
+                    const uint32_t sf_col = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS;
+                    for (int j = 0; j < nk; ++j)
+                        tc_mma(tmem, smem_desc(st + GM_A_OFF + 32 * j, 16, 1024, 2),
+                               smem_desc(st + GM_B_OFF + 32 * j, 16, 1024, 2), idesc, sf_col + 4 * j,
+                               sf_col + 16 + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+                    tc_commit(empty_bar(s));
+                    issued_any = true;
                 }
-                tc_commit(empty_bar(s));
-                issued_any = true;
+                if (*abort_flag) break;
+                tc_commit(acc_full);
             }
-            if (!*abort_flag) {
-                tc_commit(acc_bar);
-                // tensor memory is freed only after the last MMA has completed
-                for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
-                    if (mbar_try_wait(acc_bar, 0u)) break;
-            } else if (issued_any) {
-                tc_commit(drain_bar);  // completes when every MMA/copy issued so far has finished
+            // tensor memory is freed only after every MMA issued here has completed
+            if (issued_any) {
+                tc_commit(drain_bar);
                 for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
                     if (mbar_try_wait(drain_bar, 0u)) break;
             }
         }
         __syncwarp();
+    } else if (warp < 2 + GM_SF_WARPS) {
+        // ------------------------------------------------------ scale factors -> tensor memory
+        // Lane l of the quadrant-q warp writes, for tensor-memory lane 32q + l,
+        // row l of every 512-byte SF chunk of the stage (16 bytes = 4 columns).
+        const int q = warp & 3;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + GM_SF_RING;
+        uint32_t it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+            for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                const int s = (int)(it % GM_STAGES);
+                const uint32_t ph = (it / GM_STAGES) & 1u;
+                const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report(p.dev_status, BSQ_DEV_TIMEOUT);
+                    }
+                    break;
+                }
+                const uint8_t* sp = smem + (size_t)s * GM_STAGE_BYTES + 16 * lane;
+                uint32_t ra[16], rb[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 va = *reinterpret_cast<const uint4*>(sp + GM_SFA_OFF + 512 * j);
+                    const uint4 v0 = *reinterpret_cast<const uint4*>(sp + GM_SFB_OFF + 512 * j);
+                    const uint4 v1 = *reinterpret_cast<const uint4*>(sp + GM_SFB_OFF + 2048 + 512 * j);
+                    ra[4 * j] = va.x; ra[4 * j + 1] = va.y; ra[4 * j + 2] = va.z; ra[4 * j + 3] = va.w;
+                    rb[8 * j] = v0.x; rb[8 * j + 1] = v0.y; rb[8 * j + 2] = v0.z; rb[8 * j + 3] = v0.w;
+                    rb[8 * j + 4] = v1.x; rb[8 * j + 5] = v1.y; rb[8 * j + 6] = v1.z; rb[8 * j + 7] = v1.w;
+                }
+                const uint32_t col = tq + (uint32_t)s * GM_SF_STAGE_COLS;
+                tc_st16(col, ra);
+                tc_st16(col + 16, rb);
+                tc_st16(col + 32, rb + 16);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sf_bar(s));
+            }
+        }
     } else {
         // ------------------------------------------------------ epilogue
-        const int q = warp & 3;
-        const int row = m0 + 32 * q + lane;
-        const bool ok = mbar_wait(acc_bar, 0u, abort_flag);
-        if (__all_sync(0xFFFFFFFFu, ok)) {
-            tc_fence_after();
-            const bool in = row < p.m_capacity;
-            const float s = in ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + e)) : 0.0f;
-            const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
-            if (swiglu) {
-                const int I = p.N >> 1;
-                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + nt * 128;
-                for (int c = 0; c < 4; ++c) {
-                    float g[32], u[32];
-                    tc_ld32(tlane + 32 * c, g);
-                    tc_ld32(tlane + 128 + 32 * c, u);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float h0 = silu(__fmul_rn(g[2 * i], s)) * __fmul_rn(u[2 * i], s);
-                        const float h1 = silu(__fmul_rn(g[2 * i + 1], s)) * __fmul_rn(u[2 * i + 1], s);
-                        w[i] = pack_bf16x2(h0, h1);
-                    }
-                    if (in && nt * 128 + 32 * c < I) {
-                        uint4* d = reinterpret_cast<uint4*>(o + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    }
+        const int q = warp & 3;                                  // tensor-memory lane quadrant
+        const int part = (warp - 2 - GM_SF_WARPS) >> 2;          // 0..3: which 64 columns (32 h for SwiGLU)
+        const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
+        uint32_t tc = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tc) {
+            const TileInfo t = tile_info(tile);
+            const bool ok = mbar_wait(acc_full, tc & 1u, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    report(p.dev_status, BSQ_DEV_TIMEOUT);
                 }
-            } else {
-                const int n0 = nt * 256;
-                for (int c = 0; c < 4 * n_halves; ++c) {
-                    float v[32];
-                    tc_ld32(tlane + 32 * c, v);
+                break;
+            }
+            tc_fence_after();
+            const int row = t.m0 + 32 * q + lane;
+            const bool active = swiglu || part < 2 * t.n_halves;
+            uint32_t r[64];
+            if (active) {
+                if (swiglu) {  // gate columns 32*part.., up columns 128 + 32*part..
+                    tc_ld32_issue(tlane + 32 * part, r);
+                    tc_ld32_issue(tlane + 128 + 32 * part, r + 32);
+                } else {
+                    tc_ld32_issue(tlane + 64 * part, r);
+                    tc_ld32_issue(tlane + 64 * part + 32, r + 32);
+                }
+                tc_ld_wait(r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);  // accumulator handed back to the MMA warp
+            if (!active || row >= p.m_capacity) continue;
+            const float s = __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e));
+            if (swiglu) {
+                uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo +
+                                                    t.nt * 128 + 32 * part);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], s);
-                    if (!in) continue;
-                    if (p.epilogue == BSQ_EPI_F32) {
-                        float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (size_t)row * p.ldo + n0 + 32 * c);
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t w[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    } else {
-                        uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + n0 + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                              pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = 8 * i + 2 * j;
+                        w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[c]) * s, __uint_as_float(r[32 + c]) * s),
+                                           swiglu1(__uint_as_float(r[c + 1]) * s, __uint_as_float(r[33 + c]) * s));
                     }
+                    d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            } else if (p.epilogue == BSQ_EPI_F32) {
+                float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (size_t)row * p.ldo + t.nt * 256 +
+                                                      64 * part);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    d[i] = make_float4(__uint_as_float(r[4 * i]) * s, __uint_as_float(r[4 * i + 1]) * s,
+                                       __uint_as_float(r[4 * i + 2]) * s, __uint_as_float(r[4 * i + 3]) * s);
+            } else {
+                uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo +
+                                                    t.nt * 256 + 64 * part);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        w[j] = pack_bf16x2(__uint_as_float(r[8 * i + 2 * j]) * s, __uint_as_float(r[8 * i + 2 * j + 1]) * s);
+                    d[i] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-        } else if (lane == 0) {
-            *abort_flag = 1;
-            report(p.dev_status, BSQ_DEV_TIMEOUT);
         }
     }
 
@@ -413,17 +564,16 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D byte tensor [rows][row_bytes], box 128 x 128 bytes, 128-byte swizzle.
-static bool make_tmap(CUtensorMap* tm, const void* base, int64_t rows, int64_t row_bytes)
+// Tensor map of `rank` dims (dims/box innermost first, strides in bytes for
+// dims 1..rank-1).
+static bool make_tmap(CUtensorMap* tm, const void* base, CUtensorMapDataType dt, int rank, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {128u, 128u};
-    cuuint32_t estr[2] = {1u, 1u};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    return fn(tm, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -435,14 +585,48 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
         if (err != cudaSuccess) return err;
         attr_set = true;
     }
-    CUtensorMap tmA, tmB;
-    if (!make_tmap(&tmA, a.a_codes, a.m_capacity, a.K / 2)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tmB, a.b_codes, a.experts * a.N, a.K / 2)) return cudaErrorInvalidValue;
+    const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16;
+    const int64_t kb = a.K / 2;          // bytes per row of codes
+    const int64_t k64 = a.K / 64;        // SF chunks per row tile
+    CUtensorMap tmA, tmB, tmSFB;
+    {   // A: [m_capacity][K/2] bytes, box 128 x 128
+        const cuuint64_t d[2] = {(cuuint64_t)kb, (cuuint64_t)a.m_capacity};
+        const cuuint64_t s[1] = {(cuuint64_t)kb};
+        const cuuint32_t b[2] = {128u, 128u};
+        if (!make_tmap(&tmA, a.a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    if (swiglu) {
+        // B viewed as [E][2 (gate, up)][I rows][K/2 bytes]: one box = 128 gate + 128 up rows
+        const int64_t I = a.N / 2;
+        const cuuint64_t d[4] = {(cuuint64_t)kb, (cuuint64_t)I, 2u, (cuuint64_t)a.experts};
+        const cuuint64_t s[3] = {(cuuint64_t)kb, (cuuint64_t)(I * kb), (cuuint64_t)(2 * I * kb)};
+        const cuuint32_t b[4] = {128u, 128u, 2u, 1u};
+        if (!make_tmap(&tmB, a.b_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        // B's SF as u64 [E * 2 (gate, up)][I/128 row tiles][k64 * 64]: one box = the
+        // 2 KB stage run of the gate row tile and of the up row tile
+        const cuuint64_t sd[3] = {(cuuint64_t)(k64 * 64), (cuuint64_t)(I / 128), (cuuint64_t)(2 * a.experts)};
+        const cuuint64_t ss[2] = {(cuuint64_t)(k64 * 512), (cuuint64_t)((I / 128) * k64 * 512)};
+        const cuuint32_t sb[3] = {256u, 1u, 2u};
+        if (!make_tmap(&tmSFB, a.b_sf, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t d[2] = {(cuuint64_t)kb, (cuuint64_t)(a.experts * a.N)};
+        const cuuint64_t s[1] = {(cuuint64_t)kb};
+        const cuuint32_t b[2] = {128u, 256u};
+        if (!make_tmap(&tmB, a.b_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        const cuuint64_t sd[2] = {(cuuint64_t)(k64 * 64), (cuuint64_t)(a.experts * a.N / 128)};
+        const cuuint64_t ss[1] = {(cuuint64_t)(k64 * 512)};
+        const cuuint32_t sb[2] = {256u, 2u};
+        if (!make_tmap(&tmSFB, a.b_sf, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     GemmParams p;
     p.a_sf = a.a_sf;
     p.a_scale = a.a_scale;
     p.offsets = a.offsets;
-    p.b_sf = a.b_sf;
     p.b_scale = a.b_scale;
     p.out = a.out;
     p.dev_status = a.dev_status;
@@ -452,11 +636,12 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
     p.K = (int32_t)a.K;
     p.N = (int32_t)a.N;
     p.epilogue = a.epilogue;
-    p.n_tiles = a.epilogue == BSQ_EPI_SWIGLU_BF16 ? (int32_t)(a.N / 256) : (int32_t)((a.N + 255) / 256);
-    const int64_t m_tiles = (a.m_capacity + 127) / 128;
-    const int64_t grid = m_tiles * p.n_tiles;
-    if (grid == 0) return cudaSuccess;
-    k_gemm_fp4<<<(unsigned)grid, GM_THREADS, GM_SMEM_BYTES, st>>>(tmA, tmB, p);
+    p.n_tiles = swiglu ? (int32_t)(a.N / 256) : (int32_t)((a.N + 255) / 256);
+    // persistent: at most one CTA per SM, never more CTAs than the largest possible tile count
+    const int64_t max_tiles = ((a.m_capacity + 127) / 128) * p.n_tiles;
+    const int64_t grid = std::min<int64_t>(max_tiles, a.sms);
+    if (grid <= 0) return cudaSuccess;
+    k_gemm_fp4<<<(unsigned)grid, GM_THREADS, GM_SMEM_BYTES, st>>>(tmA, tmB, tmSFB, p);
     return cudaGetLastError();
 }
 

@@ -41,6 +41,7 @@ struct GemmArgs {
     void* out;
     int64_t ldo;
     int32_t* dev_status;
+    int sms;  // SMs of the current device (persistent grid size)
 };
 cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st);
 

@@ -312,29 +312,32 @@ __global__ void k_sf_pad_zero(uint8_t* __restrict__ sf, int64_t rows, int64_t co
 }
 
 // ---------------------------------------------------------------------------
-// Requant pass 1: per-column maximum of |D|, D = rn(rn(e2m1 * sf) * t).  A
-// thread owns 8 columns (one code word) and a chunk of rows.  Within a row and
-// 16-block, |D| is monotonic in the code magnitude, but columns are kept
-// separate.  Results go to colmax (bits of non-negative floats, zeroed by the
-// caller) by unsigned atomicMax.
-constexpr int RQ_ROWS_PER_CTA = 128;
+// Requant pass 1: per-column maximum of |D|, D = rn(rn(e2m1 * sf) * t), in
+// two deterministic stages.  Stage A: a thread owns 8 columns (one code word)
+// of a chunk of RQ_CHUNK rows and writes the chunk maxima to
+// part[chunk][K].  Stage B: one thread per column reduces over the chunks.
+constexpr int RQ_CHUNK = 32;
+constexpr int RQ_COLMAX_THREADS = 128;
 
 template <bool SWZ>
-__global__ void __launch_bounds__(256) k_requant_colmax(const uint8_t* __restrict__ codes,
-                                                        const uint8_t* __restrict__ sf,
-                                                        const float* __restrict__ row_scale, int64_t rows,
-                                                        int64_t K, unsigned int* __restrict__ colmax)
+__global__ void __launch_bounds__(RQ_COLMAX_THREADS) k_requant_colmax_part(const uint8_t* __restrict__ codes,
+                                                                           const uint8_t* __restrict__ sf,
+                                                                           const float* __restrict__ row_scale,
+                                                                           int64_t rows, int64_t K,
+                                                                           float* __restrict__ part)
 {
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // column group of 8
     if (g >= (K >> 3)) return;
-    const int64_t r0 = (int64_t)blockIdx.y * RQ_ROWS_PER_CTA;
-    const int64_t r1 = min(rows, r0 + RQ_ROWS_PER_CTA);
+    const int64_t r0 = (int64_t)blockIdx.y * RQ_CHUNK;
     const int64_t nsf = K >> 4;
     float m[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) m[i] = 0.0f;
     const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes);
-    for (int64_t r = r0; r < r1; ++r) {
+#pragma unroll 8
+    for (int j = 0; j < RQ_CHUNK; ++j) {
+        const int64_t r = r0 + j;
+        if (r >= rows) break;
         const uint32_t w = __ldg(cw + r * (K >> 3) + g);
         const int64_t so = SWZ ? sf_swizzled(r, g >> 1, (nsf + 3) >> 2) : r * nsf + (g >> 1);
         const float s = e4m3_to_f32(__ldg(sf + so));
@@ -345,9 +348,19 @@ __global__ void __launch_bounds__(256) k_requant_colmax(const uint8_t* __restric
             m[i] = fmaxf(m[i], __fmul_rn(__fmul_rn(a, s), t));
         }
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        if (m[i] > 0.0f) atomicMax(colmax + 8 * g + i, __float_as_uint(m[i]));
+    float4* dst = reinterpret_cast<float4*>(part + (int64_t)blockIdx.y * K + 8 * g);
+    dst[0] = make_float4(m[0], m[1], m[2], m[3]);
+    dst[1] = make_float4(m[4], m[5], m[6], m[7]);
+}
+
+__global__ void __launch_bounds__(256) k_requant_colmax_reduce(const float* __restrict__ part, int64_t nchunks,
+                                                               int64_t K, unsigned int* __restrict__ colmax)
+{
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= K) return;
+    float m = 0.0f;
+    for (int64_t j = 0; j < nchunks; ++j) m = fmaxf(m, __ldg(part + j * K + c));
+    colmax[c] = __float_as_uint(m);
 }
 
 // Requant pass 2.  CTA tile: 128 source rows (m) x 64 source columns (k),
@@ -595,10 +608,13 @@ void launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_sc
 {
     const bool nv = nvc != nullptr, mx = mxc != nullptr;
     if (nv) {
-        cudaMemsetAsync(colmax, 0, (size_t)K * sizeof(unsigned int), st);
-        dim3 g1((unsigned)(((K >> 3) + 255) / 256), (unsigned)((rows + RQ_ROWS_PER_CTA - 1) / RQ_ROWS_PER_CTA));
-        if (swz) k_requant_colmax<true><<<g1, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
-        else k_requant_colmax<false><<<g1, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
+        // workspace: colmax [K] then the per-chunk maxima [nchunks][K]
+        const int64_t nchunks = (rows + RQ_CHUNK - 1) / RQ_CHUNK;
+        float* part = reinterpret_cast<float*>(colmax) + ((K + 63) & ~(int64_t)63);
+        dim3 g1((unsigned)(((K >> 3) + RQ_COLMAX_THREADS - 1) / RQ_COLMAX_THREADS), (unsigned)nchunks);
+        if (swz) k_requant_colmax_part<true><<<g1, RQ_COLMAX_THREADS, 0, st>>>(codes, sf, row_scale, rows, K, part);
+        else k_requant_colmax_part<false><<<g1, RQ_COLMAX_THREADS, 0, st>>>(codes, sf, row_scale, rows, K, part);
+        k_requant_colmax_reduce<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(part, nchunks, K, colmax);
     }
     dim3 g2((unsigned)((K + RQ_TK - 1) / RQ_TK), (unsigned)((rows + RQ_TM - 1) / RQ_TM));
 #define BSQ_RQ(S, R, N, M)                                                                                   \

@@ -165,7 +165,8 @@ bsq_status quantize_mxfp8_rowcol(const void* x, int64_t rows, int64_t K, int64_t
  *   mx_*                   out MXFP8 of Y: codes [K][rows], sf [K][rows/32]
  *                          (both NULL: skip)
  *   workspace              device scratch of bsq_requant_workspace_size()
- *                          bytes (column maxima of |D|); may be NULL when that
+ *                          bytes (column maxima of |D| and their per-32-row
+ *                          partial maxima); may be NULL when that
  *                          size is 0
  * rows % 32 == 0, K % 16 == 0.
  * ------------------------------------------------------------------------- */

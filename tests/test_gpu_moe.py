@@ -142,7 +142,9 @@ def _staged(gpu, O, T, H, I, E, k, four_six, seed, sample_rows=None):
         yr = synth.bf16_bits_to_f32(y_ref).astype(np.float64)
         of = synth.bf16_bits_to_f32(out_gpu).astype(np.float64)
         terms = np.abs(of[slot_of.reshape(T, k)] * wts[:, :, None]).sum(axis=1)
-        assert np.all(np.abs(yg - yr) <= 2.0 ** -8 * np.abs(yr) + 1e-6 * terms + 1e-30)
+        # both sides round to bf16 independently (GPU from its fp32 sum, the
+        # oracle from fp64), so they may differ by one bf16 ulp <= 2^-7 |y|
+        assert np.all(np.abs(yg - yr) <= 2.0 ** -7 * np.abs(yr) + 1e-6 * terms + 1e-30)
     return y
 
 
