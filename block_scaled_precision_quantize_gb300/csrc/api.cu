@@ -197,6 +197,38 @@ bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const f
     return launched();
 }
 
+bsq_status requant_transpose_sr_noalloc(const uint8_t* codes, const uint8_t* sf, const float* row_scale,
+                                        int64_t rows, int64_t K, uint8_t* nv_codes_T, uint8_t* nv_sf_T,
+                                        float* nv_scale_T, uint8_t* mx_codes_T, uint8_t* mx_sf_T, uint64_t seed,
+                                        uint32_t flags, int32_t* dev_status, bsq_stream_t stream)
+{
+    (void)dev_status;
+    if (flags & ~(BSQ_SF_SWIZZLED | BSQ_STOCHASTIC)) return BSQ_ERR_FLAGS;
+    if (rows < 0 || K <= 0 || rows % 32 != 0 || K % 16 != 0 || rows > (int64_t)1 << 31) return BSQ_ERR_SHAPE;
+    if (K > noalloc_requant_max_k()) return BSQ_ERR_SHAPE;  // beyond the library's fixed scratch array
+    if (rows == 0) return BSQ_OK;
+    const bool nv = nv_codes_T || nv_sf_T || nv_scale_T;
+    const bool mx = mx_codes_T || mx_sf_T;
+    if (!codes || !sf || !row_scale) return BSQ_ERR_NULL;
+    if (!nv && !mx) return BSQ_ERR_NULL;
+    if (nv && (!nv_codes_T || !nv_sf_T || !nv_scale_T)) return BSQ_ERR_NULL;
+    if (mx && (!mx_codes_T || !mx_sf_T)) return BSQ_ERR_NULL;
+    if (!a16(codes) || (nv && !a16(nv_codes_T)) || (mx && !a16(mx_codes_T))) return BSQ_ERR_ALIGN;
+    int sms;
+    bsq_status st = current_device(&sms);
+    if (st != BSQ_OK) return st;
+    const bool swz = (flags & BSQ_SF_SWIZZLED) != 0;
+    if (launch_requant_noalloc(codes, sf, row_scale, rows, K, nv ? nv_codes_T : nullptr, nv_sf_T, nv_scale_T,
+                               mx ? mx_codes_T : nullptr, mx_sf_T, seed, (flags & BSQ_STOCHASTIC) != 0, swz,
+                               stream) != cudaSuccess)
+        return BSQ_ERR_CUDA;
+    if (swz) {
+        if (nv) launch_sf_pad_zero(nv_sf_T, K, rows / 16, sms, stream);
+        if (mx) launch_sf_pad_zero(mx_sf_T, K, rows / 32, sms, stream);
+    }
+    return launched();
+}
+
 bsq_status grouped_expert_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
                                    const int32_t* offsets, int64_t experts, int64_t m_capacity, int64_t K, int64_t N,
                                    const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,

@@ -18,6 +18,10 @@ void launch_sf_pad_zero(uint8_t* sf, int64_t rows, int64_t cols, int sms, cudaSt
 void launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
                     unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
                     uint64_t seed, bool sr, bool swz, cudaStream_t st);
+int64_t noalloc_requant_max_k();
+cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
+                                   int64_t K, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
+                                   uint64_t seed, bool sr, bool swz, cudaStream_t st);
 void launch_sf_swizzle(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, int dir, int sms,
                        cudaStream_t st);
 void launch_format_probe(int kind, const float* in, const uint32_t* rbits, void* out, int64_t n, int sms,

@@ -8,6 +8,8 @@
 // integer operations on bf16 magnitude bits and warp shuffles, and writes
 // packed codes with 8- to 32-byte stores.  Grids are sized in multiples of
 // the SM count.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -651,6 +653,118 @@ void launch_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t
                           cudaStream_t st)
 {
     k_philox_bits16<<<sms * 8, 256, 0, st>>>(seed, stream, idx0, n, out);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free requantization (requant_transpose_sr_noalloc).
+//
+// Some callers cannot give the library device memory for scratch: a host
+// framework that only owns its input and output buffers, or code that must
+// not allocate device memory once it is running.  For them the column maxima
+// of |D| live in this file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds it (256 KB) until the process exits,
+// every call shares it, and it keeps the last call's contents, so each call
+// clears the part it uses first; calls that overlap on the GPU (different
+// streams, or different host threads on one device) race on it.
+namespace {
+
+constexpr int64_t kNoallocMaxK = 65536;
+constexpr int kNoallocRows = 64;  // rows per CTA of the column-maximum pass
+__device__ __align__(256) unsigned int g_requant_colmax[kNoallocMaxK];
+
+// Column maxima of |D| straight into the shared array: a thread owns 8
+// columns of kNoallocRows rows and folds them in with unsigned atomicMax on
+// the bits of non-negative floats (order-independent, so deterministic).
+template <bool SWZ>
+__global__ void __launch_bounds__(128) k_requant_colmax_atomic(const uint8_t* __restrict__ codes,
+                                                               const uint8_t* __restrict__ sf,
+                                                               const float* __restrict__ row_scale, int64_t rows,
+                                                               int64_t K, unsigned int* __restrict__ colmax)
+{
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= (K >> 3)) return;
+    const int64_t r0 = (int64_t)blockIdx.y * kNoallocRows;
+    const int64_t nsf = K >> 4;
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = 0.0f;
+    const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes);
+#pragma unroll 8
+    for (int j = 0; j < kNoallocRows; ++j) {
+        const int64_t r = r0 + j;
+        if (r >= rows) break;
+        const uint32_t w = __ldg(cw + r * (K >> 3) + g);
+        const int64_t so = SWZ ? sf_swizzled(r, g >> 1, (nsf + 3) >> 2) : r * nsf + (g >> 1);
+        const float s = e4m3_to_f32(__ldg(sf + so));
+        const float t = __ldg(row_scale + r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], __fmul_rn(__fmul_rn(e2m1_to_f32((w >> (4 * i)) & 7u), s), t));
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (m[i] > 0.0f) atomicMax(colmax + 8 * g + i, __float_as_uint(m[i]));
+}
+
+// Device address of g_requant_colmax, looked up once per device with that
+// device current (the host-side name is only a stand-in for it).
+constexpr int kNoallocDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned int* g_noalloc_ptr[kNoallocDevices];
+
+cudaError_t noalloc_scratch(unsigned int** out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kNoallocDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_requant_colmax);
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int64_t noalloc_requant_max_k() { return kNoallocMaxK; }
+
+cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
+                                   int64_t K, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
+                                   uint64_t seed, bool sr, bool swz, cudaStream_t st)
+{
+    unsigned int* colmax = nullptr;
+    cudaError_t err = noalloc_scratch(&colmax);
+    if (err != cudaSuccess) return err;
+    const bool nv = nvc != nullptr, mx = mxc != nullptr;
+    if (nv) {
+        err = cudaMemsetAsync(colmax, 0, (size_t)K * sizeof(unsigned int), st);
+        if (err != cudaSuccess) return err;
+        dim3 g1((unsigned)(((K >> 3) + 127) / 128), (unsigned)((rows + kNoallocRows - 1) / kNoallocRows));
+        if (swz) k_requant_colmax_atomic<true><<<g1, 128, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
+        else k_requant_colmax_atomic<false><<<g1, 128, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
+    }
+    dim3 g2((unsigned)((K + RQ_TK - 1) / RQ_TK), (unsigned)((rows + RQ_TM - 1) / RQ_TM));
+#define BSQ_RQN(S, R, N, M)                                                                                   \
+    k_requant_main<S, R, N, M><<<g2, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, \
+                                                   seed)
+#define BSQ_RQN2(S, R)                            \
+    do {                                          \
+        if (nv && mx) BSQ_RQN(S, R, true, true);  \
+        else if (nv) BSQ_RQN(S, R, true, false);  \
+        else BSQ_RQN(S, R, false, true);          \
+    } while (0)
+    if (swz) {
+        if (sr) BSQ_RQN2(true, true); else BSQ_RQN2(true, false);
+    } else {
+        if (sr) BSQ_RQN2(false, true); else BSQ_RQN2(false, false);
+    }
+#undef BSQ_RQN2
+#undef BSQ_RQN
+    return cudaGetLastError();
 }
 
 }  // namespace bsq

@@ -179,6 +179,32 @@ bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const f
                                 uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * requant_transpose_sr_noalloc: requant_transpose_sr for callers that cannot
+ * hand the library device scratch memory -- a host framework that owns only
+ * its input and output buffers, or code that must not allocate device memory
+ * once it is running.  (The source pages have no counterpart; this is an
+ * interface convenience.)  Same arguments, layouts and results as
+ * requant_transpose_sr, without the workspace: the column maxima of the
+ * NVFP4 target live in a 256 KB array inside the library that every GPU
+ * loading the library keeps until the process exits.  The function calls no
+ * allocator.
+ *   - K must be <= 65536; larger K is rejected with BSQ_ERR_SHAPE before
+ *     anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before capturing the
+ *     stream into a graph.
+ *   - Every call on a device uses the same array and clears the part it
+ *     needs first; calls whose GPU work overlaps (other streams, other host
+ *     threads on the same device) race on it and must be serialized by the
+ *     caller.
+ * ------------------------------------------------------------------------- */
+bsq_status requant_transpose_sr_noalloc(const uint8_t* codes, const uint8_t* sf, const float* row_scale,
+                                        int64_t rows, int64_t K,
+                                        uint8_t* nv_codes_T, uint8_t* nv_sf_T, float* nv_scale_T,
+                                        uint8_t* mx_codes_T, uint8_t* mx_sf_T,
+                                        uint64_t seed, uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * grouped_expert_gemm_fp4: block-scaled grouped GEMM on the tensor cores
  * (kind::mxf4nvf4, E4M3 scale per 16 elements) with the FP32 rescale fused in
  * the epilogue ("LMSYS Drops Miles ...", "Why Blackwell changes the math":
