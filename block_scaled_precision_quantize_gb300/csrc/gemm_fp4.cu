@@ -15,24 +15,34 @@
 // Persistent kernel, one CTA per SM.  The grouped problem is flattened into
 // 128-row x 256-column output tiles (128-row tiles of the expert-sorted A,
 // each inside one expert's segment, times the N tiles), walked round-robin.
-// On sm_103 a single thread issuing tcgen05 instructions needs ~100+ cycles
-// per instruction, about what one 128x256x64 FP4 MMA computes, so the design
-// keeps that thread's instruction stream down to the MMAs themselves:
-//   warp 0      TMA producer, 4 copies per 256-wide K stage: A (128 x 128 B),
-//               B (256 rows: one 2-D box, or gate + up blocks in one 4-D box
-//               for SwiGLU), A's SF (one 2 KB bulk copy) and B's SF (two
-//               512-byte-chunk runs in one 2-D/3-D box of u64 elements)
-//   warp 1      allocates tensor memory; one lane issues one
-//               128 x 256 x 64 MMA per K step and the commits
-//   warps 2-5   one per tensor-memory lane quadrant: copy each stage's scale
-//               factors from shared into tensor memory with tcgen05.st (the
-//               layout tcgen05.cp 32x128b.warpx4 would produce: every
-//               quadrant holds the 32 x 16-byte chunk rows), then signal
+// One 128 x 256 x 64 FP4 MMA occupies the tensor core for 128 cycles, so a
+// 256-wide K stage (4 MMAs, 54 KB of operands and scale factors) must arrive
+// every ~512 cycles: the kernel is fed by the TMA engine at close to its
+// per-SM rate, and everything else is arranged to stay off that path.
+//   warp 0      TMA producer.  Per stage it first copies the scale factors
+//               (A's: one 2 KB bulk copy; B's: two 512-byte-chunk runs in one
+//               2-D/3-D box of u64 elements) on their own barrier, then the
+//               codes: A (128 x 128 B) and B (256 rows: one 2-D box, or the
+//               gate + up blocks in one 4-D box for SwiGLU)
+//   warp 1      allocates tensor memory; one lane issues one 128 x 256 x 64
+//               MMA per K step and the commits.  It touches shared memory only
+//               for its barrier waits (a tile's width is all it needs to know)
+//   warps 2-5   one per tensor-memory lane quadrant: as soon as a stage's
+//               scale factors land, copy them into tensor memory with
+//               tcgen05.st while the codes are still in flight.  B's chunks are
+//               replicated in every quadrant (the layout tcgen05.cp
+//               32x128b.warpx4 produces); for A, the lanes of quadrant q read
+//               only column q of each 4-column chunk group (rows 32q + l), so
+//               one 4-byte word per chunk row is enough
 //   warps 6-21  epilogue, four warps per lane quadrant, 64 columns each: load
-//               the accumulator, hand it back to the MMA warp at once, then
-//               rescale / SwiGLU / store while the next tile's MMAs run
+//               the accumulator, hand it back to the MMA warp, then rescale /
+//               SwiGLU / store while the next tile's MMAs run
 // Shared memory: GM_STAGES stages of [SFA 2 KB][SFB 4 KB][A 16 KB][B 32 KB]
-// (A and B 128-byte swizzled, 1024-byte aligned) and the expert offsets.
+// (A and B 128-byte swizzled, 1024-byte aligned), the expert offsets, and a
+// 2 KB staging buffer per epilogue warp.  A warp holds 32 output rows (one per
+// thread); for bf16 outputs it writes each 32 x 32 block into its buffer and
+// one lane stores it with a TMA tensor store: one global store instruction
+// per 2 KB instead of 128 scattered 16-byte stores.
 // Tensor memory: 512 columns = accumulator (256) + an SF ring (48 per stage:
 // SFA k-step j at 4j, SFB k-step j at 16 + 8j, both N halves side by side).
 // Every mbarrier wait is bounded; on expiry the CTA records BSQ_DEV_TIMEOUT,
@@ -48,7 +58,7 @@ namespace bsq {
 constexpr int GM_SF_WARPS = 4;
 constexpr int GM_EPI_WARPS = 16;
 constexpr int GM_THREADS = 32 * (2 + GM_SF_WARPS + GM_EPI_WARPS);  // 704
-constexpr int GM_STAGES = 4;
+constexpr int GM_STAGES = 3;
 constexpr int GM_SFA_OFF = 0;
 constexpr int GM_SFB_OFF = 2048;
 constexpr int GM_A_OFF = 6144;
@@ -57,9 +67,11 @@ constexpr int GM_STAGE_BYTES = 6144 + 16384 + 32768;  // 55296 = 54 KB
 constexpr int GM_TMEM_COLS = 512;
 constexpr int GM_SF_RING = 256;                       // first SF column
 constexpr int GM_SF_STAGE_COLS = 48;
-constexpr int GM_MAX_SMEM_EXPERTS = 1024;             // offsets cached in shared memory up to this E
+constexpr int GM_MAX_SMEM_EXPERTS = 256;              // offsets cached in shared memory up to this E
 constexpr uint32_t GM_SPIN_LIMIT = 1u << 22;
-constexpr size_t GM_SMEM_BYTES = (size_t)GM_STAGES * GM_STAGE_BYTES + 1024;
+constexpr int GM_EPI_OFF = GM_STAGES * GM_STAGE_BYTES;        // epilogue staging, per warp
+constexpr int GM_EPI_WARP_BYTES = 32 * 64;                     // 32 rows x 64 bytes, 64-byte swizzled
+constexpr size_t GM_SMEM_BYTES = (size_t)GM_EPI_OFF + (size_t)GM_EPI_WARPS * GM_EPI_WARP_BYTES + 1024;
 
 // Instruction descriptors, kind::mxf4nvf4: A and B are E2M1 (format 1),
 // K-major, no negation, N>>3 at bit 17, M = 128 (M>>4 at bit 24), scale type
@@ -235,9 +247,39 @@ BSQ_DEVICE void tc_st16(uint32_t taddr, const uint32_t* r)
 // e^-g -> inf limit gives h -> 0.
 BSQ_DEVICE float swiglu1(float g, float u) { return __fdividef(g * u, 1.0f + __expf(-g)); }
 
+// The epilogue's bf16 block store: thread `lane` owns row `lane` of a 32 x 32
+// bf16 block (64 bytes).  The warp's buffer uses the TMA 64-byte swizzle
+// (16-byte chunk c of row r lives at chunk c ^ ((r >> 1) & 3)), which also
+// keeps the 16-byte writes of each quarter-warp on distinct banks; one lane
+// then stores the block with a TMA tensor store (rows past the tensor map's
+// extent are clipped by the hardware).
+BSQ_DEVICE void stage_put(uint8_t* buf, int lane, int c, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3)
+{
+    *reinterpret_cast<uint4*>(buf + 64 * lane + 16 * (c ^ ((lane >> 1) & 3))) = make_uint4(w0, w1, w2, w3);
+}
+BSQ_DEVICE void stage_store(const uint8_t* buf, int lane, const CUtensorMap* tm, int x, int y)
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                         reinterpret_cast<uint64_t>(tm)),
+                     "r"(x), "r"(y), "r"(smem_u32(buf))
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+// The buffer may be rewritten once the previous store has read it.
+BSQ_DEVICE void stage_reuse(int lane)
+{
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------ kernel
 struct GemmParams {
     const uint8_t* a_sf;
+    const uint8_t* b_sf;
     const float* a_scale;
     const int32_t* offsets;
     const float* b_scale;
@@ -256,12 +298,16 @@ struct TileInfo {
     int m0, nt, e, n_halves;
 };
 
+// EPI is the epilogue (BSQ_EPI_*): one instantiation per epilogue keeps each
+// one's register allocation to its own path.
+template <int EPI>
 __global__ void __launch_bounds__(GM_THREADS, 1)
     k_gemm_fp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmSFB, const GemmParams p)
+               const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmOut,
+               const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[3 * GM_STAGES + 3];
+    __shared__ __align__(8) uint64_t bars[4 * GM_STAGES + 3];
     __shared__ int32_t s_off[GM_MAX_SMEM_EXPERTS + 1];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort, s_bad;
@@ -277,15 +323,17 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(GM_STAGES + s); };
     auto sf_bar = [&](int s) { return bar0 + 8u * (uint32_t)(2 * GM_STAGES + s); };
-    const uint32_t acc_full = bar0 + 8u * (3 * GM_STAGES);
-    const uint32_t acc_empty = bar0 + 8u * (3 * GM_STAGES + 1);
-    const uint32_t drain_bar = bar0 + 8u * (3 * GM_STAGES + 2);
+    auto sf_full = [&](int s) { return bar0 + 8u * (uint32_t)(3 * GM_STAGES + s); };
+    const uint32_t acc_full = bar0 + 8u * (4 * GM_STAGES);
+    const uint32_t acc_empty = bar0 + 8u * (4 * GM_STAGES + 1);
+    const uint32_t drain_bar = bar0 + 8u * (4 * GM_STAGES + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < GM_STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
             mbar_init(sf_bar(s), GM_SF_WARPS);
+            mbar_init(sf_full(s), 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, GM_EPI_WARPS);
@@ -321,7 +369,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
     __syncthreads();
 
-    const bool swiglu = p.epilogue == BSQ_EPI_SWIGLU_BF16;
+    constexpr bool swiglu = EPI == BSQ_EPI_SWIGLU_BF16;
     const int k64_total = p.K >> 6;
     const int kt_count = (k64_total + 3) >> 2;
     const int m_tiles = s_bad ? 0 : (off(E) + 127) >> 7;
@@ -359,26 +407,33 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                         report(p.dev_status, BSQ_DEV_TIMEOUT);
                         break;
                     }
-                    const int nk = min(4, k64_total - 4 * kt);
                     const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
+                    const int nk = min(4, k64_total - 4 * kt);
+                    // the scale factors first, on their own barrier, so the SF warps can
+                    // move them into tensor memory while the codes are still arriving;
                     // boxes always deliver their full size (out-of-range parts are zero-filled)
-                    mbar_expect_tx(full_bar(s), 16384u + 32768u + 4096u + (uint32_t)nk * 512u);
+                    mbar_expect_tx(sf_full(s), 4096u + (uint32_t)nk * 512u);
+                    if (swiglu)
+                        tma_load_3d(st + GM_SFB_OFF, &tmSFB, kt * 256, t.nt, 2 * t.e, sf_full(s));
+                    else
+                        tma_load_2d(st + GM_SFB_OFF, &tmSFB, kt * 256, (t.e * p.N + t.nt * 256) >> 7, sf_full(s));
+                    bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 2048, (uint32_t)nk * 512u, sf_full(s));
+                    mbar_expect_tx(full_bar(s), 16384u + 32768u);
                     tma_load_2d(st + GM_A_OFF, &tmA, kt * 128, t.m0, full_bar(s));
-                    if (swiglu) {
+                    if (swiglu)
                         tma_load_4d(st + GM_B_OFF, &tmB, kt * 128, t.nt * 128, 0, t.e, full_bar(s));
-                        tma_load_3d(st + GM_SFB_OFF, &tmSFB, kt * 256, t.nt, 2 * t.e, full_bar(s));
-                    } else {
+                    else
                         tma_load_2d(st + GM_B_OFF, &tmB, kt * 128, t.e * p.N + t.nt * 256, full_bar(s));
-                        tma_load_2d(st + GM_SFB_OFF, &tmSFB, kt * 256, (t.e * p.N + t.nt * 256) >> 7, full_bar(s));
-                    }
-                    bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 2048, (uint32_t)nk * 512u, full_bar(s));
                 }
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA exits
-                for (uint32_t j = (it > GM_STAGES ? it - GM_STAGES : 0u); j < it; ++j)
+                for (uint32_t j = (it > GM_STAGES ? it - GM_STAGES : 0u); j < it; ++j) {
                     for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
                         if (mbar_try_wait(full_bar((int)(j % GM_STAGES)), (j / GM_STAGES) & 1u)) break;
+                    for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
+                        if (mbar_try_wait(sf_full((int)(j % GM_STAGES)), (j / GM_STAGES) & 1u)) break;
+                }
             }
         }
     } else if (warp == 1) {
@@ -386,9 +441,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0, tc = 0;
             bool issued_any = false;
+            const uint64_t adesc0 = smem_desc(sbase + GM_A_OFF, 16, 1024, 2);
+            const uint64_t bdesc0 = smem_desc(sbase + GM_B_OFF, 16, 1024, 2);
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++tc) {
-                const TileInfo t = tile_info(tile);
-                const uint32_t idesc = gm_idesc(t.n_halves == 2 ? 256u : 128u);
+                // only the tile's width matters here (no expert lookup: shared-memory
+                // loads from this thread are slow while the copies stream in)
+                const int nt = tile % p.n_tiles;
+                const uint32_t idesc = gm_idesc((swiglu || nt * 256 + 128 < p.N) ? 256u : 128u);
                 // the epilogue has taken the previous accumulator out of tensor memory
                 if (!mbar_wait(acc_empty, (tc & 1u) ^ 1u, abort_flag)) {
                     *abort_flag = 1;
@@ -399,19 +458,25 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = (int)(it % GM_STAGES);
                     const uint32_t ph = (it / GM_STAGES) & 1u;
-                    if (!mbar_wait(sf_bar(s), ph, abort_flag)) {  // implies the stage's data has landed
+                    // codes landed (TMA) and scale factors staged in tensor memory (SF warps)
+                    bool ok = mbar_wait(full_bar(s), ph, abort_flag);
+                    ok = ok && mbar_wait(sf_bar(s), ph, abort_flag);
+                    if (!ok) {
                         *abort_flag = 1;
                         report(p.dev_status, BSQ_DEV_TIMEOUT);
                         break;
                     }
                     tc_fence_after();
                     const int nk = min(4, k64_total - 4 * kt);
-                    const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
+                    // descriptors advance 32 bytes (2 in the >>4 address field) per K step
+                    const uint64_t ad = adesc0 + (uint64_t)s * (GM_STAGE_BYTES >> 4);
+                    const uint64_t bd = bdesc0 + (uint64_t)s * (GM_STAGE_BYTES >> 4);
                     const uint32_t sf_col = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS;
-                    for (int j = 0; j < nk; ++j)
-                        tc_mma(tmem, smem_desc(st + GM_A_OFF + 32 * j, 16, 1024, 2),
-                               smem_desc(st + GM_B_OFF + 32 * j, 16, 1024, 2), idesc, sf_col + 4 * j,
-                               sf_col + 16 + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (j < nk)
+                            tc_mma(tmem, ad + 2 * j, bd + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                                   (kt > 0 || j > 0) ? 1u : 0u);
                     tc_commit(empty_bar(s));
                     issued_any = true;
                 }
@@ -430,6 +495,8 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         // ------------------------------------------------------ scale factors -> tensor memory
         // Lane l of the quadrant-q warp writes, for tensor-memory lane 32q + l,
         // row l of every 512-byte SF chunk of the stage (16 bytes = 4 columns).
+        // The SF copies have their own barrier and are issued before the
+        // stage's codes, so this runs while the codes are still in flight.
         const int q = warp & 3;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + GM_SF_RING;
         uint32_t it = 0;
@@ -437,7 +504,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             for (int kt = 0; kt < kt_count; ++kt, ++it) {
                 const int s = (int)(it % GM_STAGES);
                 const uint32_t ph = (it / GM_STAGES) & 1u;
-                const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
+                // implies the slot's previous scale factors were consumed: the producer
+                // refills a stage only after the MMAs that read it completed
+                const bool ok = mbar_wait(sf_full(s), ph, abort_flag);
                 if (!__all_sync(0xFFFFFFFFu, ok)) {
                     if (lane == 0) {
                         *abort_flag = 1;
@@ -445,14 +514,18 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                     }
                     break;
                 }
+                tc_fence_after();
                 const uint8_t* sp = smem + (size_t)s * GM_STAGE_BYTES + 16 * lane;
                 uint32_t ra[16], rb[32];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint4 va = *reinterpret_cast<const uint4*>(sp + GM_SFA_OFF + 512 * j);
+                    // A: chunk row l holds rows l, l+32, l+64, l+96 in its four
+                    // columns, and the quadrant-q lanes (rows 32q + l) read only
+                    // column q, so one 4-byte word per chunk fills this quadrant
+                    const uint32_t va = *reinterpret_cast<const uint32_t*>(sp + GM_SFA_OFF + 512 * j + 4 * q);
                     const uint4 v0 = *reinterpret_cast<const uint4*>(sp + GM_SFB_OFF + 512 * j);
                     const uint4 v1 = *reinterpret_cast<const uint4*>(sp + GM_SFB_OFF + 2048 + 512 * j);
-                    ra[4 * j] = va.x; ra[4 * j + 1] = va.y; ra[4 * j + 2] = va.z; ra[4 * j + 3] = va.w;
+                    ra[4 * j] = va; ra[4 * j + 1] = va; ra[4 * j + 2] = va; ra[4 * j + 3] = va;
                     rb[8 * j] = v0.x; rb[8 * j + 1] = v0.y; rb[8 * j + 2] = v0.z; rb[8 * j + 3] = v0.w;
                     rb[8 * j + 4] = v1.x; rb[8 * j + 5] = v1.y; rb[8 * j + 6] = v1.z; rb[8 * j + 7] = v1.w;
                 }
@@ -471,6 +544,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int q = warp & 3;                                  // tensor-memory lane quadrant
         const int part = (warp - 2 - GM_SF_WARPS) >> 2;          // 0..3: which 64 columns (32 h for SwiGLU)
         const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
+        uint8_t* stage_buf = smem + GM_EPI_OFF + (warp - 2 - GM_SF_WARPS) * GM_EPI_WARP_BYTES;
         uint32_t tc = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tc) {
             const TileInfo t = tile_info(tile);
@@ -485,6 +559,36 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             tc_fence_after();
             const int row = t.m0 + 32 * q + lane;
             const bool active = swiglu || part < 2 * t.n_halves;
+            if constexpr (EPI == BSQ_EPI_BF16) {
+                // two rounds of 32 columns (only 32 accumulator words live at a
+                // time); the accumulator goes back after the second load
+                const float s = (active && row < p.m_capacity) ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e)) : 0.0f;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t r[32];
+                    if (active) {
+                        tc_ld32_issue(tlane + 64 * part + 32 * h2, r);
+                        tc_ld_wait(r);
+                    }
+                    if (h2 == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                    }
+                    if (!active) continue;
+                    stage_reuse(lane);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t* v = r + 8 * c;
+                        stage_put(stage_buf, lane, c, pack_bf16x2(__uint_as_float(v[0]) * s, __uint_as_float(v[1]) * s),
+                                  pack_bf16x2(__uint_as_float(v[2]) * s, __uint_as_float(v[3]) * s),
+                                  pack_bf16x2(__uint_as_float(v[4]) * s, __uint_as_float(v[5]) * s),
+                                  pack_bf16x2(__uint_as_float(v[6]) * s, __uint_as_float(v[7]) * s));
+                    }
+                    stage_store(stage_buf, lane, &tmOut, t.nt * 256 + 64 * part + 32 * h2, t.m0 + 32 * q);
+                }
+                continue;
+            }
             uint32_t r[64];
             if (active) {
                 if (swiglu) {  // gate columns 32*part.., up columns 128 + 32*part..
@@ -499,42 +603,33 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);  // accumulator handed back to the MMA warp
-            if (!active || row >= p.m_capacity) continue;
-            const float s = __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e));
-            if (swiglu) {
-                uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo +
-                                                    t.nt * 128 + 32 * part);
+            if (!active) continue;
+            const float s = (row < p.m_capacity) ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e)) : 0.0f;
+            if constexpr (swiglu) {
+                stage_reuse(lane);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int c = 0; c < 32; c += 8) {
                     uint32_t w[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int c = 8 * i + 2 * j;
-                        w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[c]) * s, __uint_as_float(r[32 + c]) * s),
-                                           swiglu1(__uint_as_float(r[c + 1]) * s, __uint_as_float(r[33 + c]) * s));
+                        const int g = c + 2 * j;
+                        w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[g]) * s, __uint_as_float(r[32 + g]) * s),
+                                           swiglu1(__uint_as_float(r[g + 1]) * s, __uint_as_float(r[33 + g]) * s));
                     }
-                    d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    stage_put(stage_buf, lane, c >> 3, w[0], w[1], w[2], w[3]);
                 }
-            } else if (p.epilogue == BSQ_EPI_F32) {
+                stage_store(stage_buf, lane, &tmOut, t.nt * 128 + 32 * part, t.m0 + 32 * q);
+            } else if (row < p.m_capacity) {
                 float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (size_t)row * p.ldo + t.nt * 256 +
                                                       64 * part);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     d[i] = make_float4(__uint_as_float(r[4 * i]) * s, __uint_as_float(r[4 * i + 1]) * s,
                                        __uint_as_float(r[4 * i + 2]) * s, __uint_as_float(r[4 * i + 3]) * s);
-            } else {
-                uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo +
-                                                    t.nt * 256 + 64 * part);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        w[j] = pack_bf16x2(__uint_as_float(r[8 * i + 2 * j]) * s, __uint_as_float(r[8 * i + 2 * j + 1]) * s);
-                    d[i] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
             }
         }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -581,8 +676,10 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(k_gemm_fp4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM_BYTES);
-        if (err != cudaSuccess) return err;
+        for (auto fn : {k_gemm_fp4<BSQ_EPI_F32>, k_gemm_fp4<BSQ_EPI_BF16>, k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>}) {
+            cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM_BYTES);
+            if (err != cudaSuccess) return err;
+        }
         attr_set = true;
     }
     const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16;
@@ -617,14 +714,28 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
         const cuuint32_t b[2] = {128u, 256u};
         if (!make_tmap(&tmB, a.b_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
+        // B's SF as u64 [E*N/128 row tiles][k64 * 64]: one box = the 2 KB stage runs of two row tiles
         const cuuint64_t sd[2] = {(cuuint64_t)(k64 * 64), (cuuint64_t)(a.experts * a.N / 128)};
         const cuuint64_t ss[1] = {(cuuint64_t)(k64 * 512)};
         const cuuint32_t sb[2] = {256u, 2u};
         if (!make_tmap(&tmSFB, a.b_sf, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
+    CUtensorMap tmOut;
+    if (a.epilogue == BSQ_EPI_F32) {
+        memset(&tmOut, 0, sizeof(tmOut));  // f32 output is stored directly
+    } else {
+        // bf16 output [m_capacity][ncols] with row pitch ldo: 32 x 32 boxes, 64-byte swizzle
+        const int64_t ncols = swiglu ? a.N / 2 : a.N;
+        const cuuint64_t d[2] = {(cuuint64_t)ncols, (cuuint64_t)a.m_capacity};
+        const cuuint64_t s[1] = {(cuuint64_t)(a.ldo * 2)};
+        const cuuint32_t b[2] = {32u, 32u};
+        if (!make_tmap(&tmOut, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, s, b, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    }
     GemmParams p;
     p.a_sf = a.a_sf;
+    p.b_sf = a.b_sf;
     p.a_scale = a.a_scale;
     p.offsets = a.offsets;
     p.b_scale = a.b_scale;
@@ -641,7 +752,9 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
     const int64_t max_tiles = ((a.m_capacity + 127) / 128) * p.n_tiles;
     const int64_t grid = std::min<int64_t>(max_tiles, a.sms);
     if (grid <= 0) return cudaSuccess;
-    k_gemm_fp4<<<(unsigned)grid, GM_THREADS, GM_SMEM_BYTES, st>>>(tmA, tmB, tmSFB, p);
+    auto kern = swiglu ? k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>
+                       : (a.epilogue == BSQ_EPI_BF16 ? k_gemm_fp4<BSQ_EPI_BF16> : k_gemm_fp4<BSQ_EPI_F32>);
+    kern<<<(unsigned)grid, GM_THREADS, GM_SMEM_BYTES, st>>>(tmA, tmB, tmSFB, tmOut, p);
     return cudaGetLastError();
 }
 
