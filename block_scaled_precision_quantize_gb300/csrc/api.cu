@@ -42,6 +42,7 @@ bsq_status current_device(int* sms)
 }
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool a4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bsq_status launched()
 {
@@ -159,9 +160,8 @@ bsq_status quantize_mxfp8_rowcol(const void* x, int64_t rows, int64_t K, int64_t
 size_t bsq_requant_workspace_size(int64_t rows, int64_t K, int32_t nvfp4_target)
 {
     if (!nvfp4_target || K <= 0 || rows <= 0) return 0;
-    // column maxima [K] (padded to 64) + per-32-row-chunk maxima [ceil(rows/32)][K]
-    const size_t nchunks = (size_t)((rows + 31) / 32);
-    return align256(((size_t)((K + 63) & ~(int64_t)63) + nchunks * (size_t)K) * sizeof(float));
+    // the column maxima of |D| (K words, padded to 64)
+    return align256((size_t)((K + 63) & ~(int64_t)63) * sizeof(float));
 }
 
 bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
@@ -181,15 +181,17 @@ bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const f
     if (nv && (!nv_codes_T || !nv_sf_T || !nv_scale_T)) return BSQ_ERR_NULL;
     if (mx && (!mx_codes_T || !mx_sf_T)) return BSQ_ERR_NULL;
     if (!a16(codes) || (nv && !a16(nv_codes_T)) || (mx && !a16(mx_codes_T))) return BSQ_ERR_ALIGN;
+    if (!a4(sf) || (nv && !a4(nv_sf_T)) || (mx && !a4(mx_sf_T))) return BSQ_ERR_ALIGN;
     const size_t need = bsq_requant_workspace_size(rows, K, nv ? 1 : 0);
     if (need && (!workspace || workspace_bytes < need)) return BSQ_ERR_WORKSPACE;
     int sms;
     bsq_status st = current_device(&sms);
     if (st != BSQ_OK) return st;
     const bool swz = (flags & BSQ_SF_SWIZZLED) != 0;
-    launch_requant(codes, sf, row_scale, rows, K, static_cast<unsigned int*>(workspace), nv ? nv_codes_T : nullptr,
-                   nv_sf_T, nv_scale_T, mx ? mx_codes_T : nullptr, mx_sf_T, seed, (flags & BSQ_STOCHASTIC) != 0, swz,
-                   stream);
+    if (launch_requant(codes, sf, row_scale, rows, K, static_cast<unsigned int*>(workspace), nv ? nv_codes_T : nullptr,
+                       nv_sf_T, nv_scale_T, mx ? mx_codes_T : nullptr, mx_sf_T, seed, (flags & BSQ_STOCHASTIC) != 0,
+                       swz, stream) != cudaSuccess)
+        return BSQ_ERR_CUDA;
     if (swz) {
         if (nv) launch_sf_pad_zero(nv_sf_T, K, rows / 16, sms, stream);
         if (mx) launch_sf_pad_zero(mx_sf_T, K, rows / 32, sms, stream);
@@ -214,6 +216,7 @@ bsq_status requant_transpose_sr_noalloc(const uint8_t* codes, const uint8_t* sf,
     if (nv && (!nv_codes_T || !nv_sf_T || !nv_scale_T)) return BSQ_ERR_NULL;
     if (mx && (!mx_codes_T || !mx_sf_T)) return BSQ_ERR_NULL;
     if (!a16(codes) || (nv && !a16(nv_codes_T)) || (mx && !a16(mx_codes_T))) return BSQ_ERR_ALIGN;
+    if (!a4(sf) || (nv && !a4(nv_sf_T)) || (mx && !a4(mx_sf_T))) return BSQ_ERR_ALIGN;
     int sms;
     bsq_status st = current_device(&sms);
     if (st != BSQ_OK) return st;

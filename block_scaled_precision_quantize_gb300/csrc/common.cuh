@@ -11,6 +11,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -68,6 +69,36 @@ BSQ_DEVICE float e2m1_to_f32(uint32_t nib)
     return __uint_as_float(bits | ((nib & 8u) << 28));
 }
 
+// Eight E2M1 codes (nibble i = element i) times one E4M3 scale factor, as
+// four f16x2 pairs (element 2i in the low half of h[i]), exactly: E2M1 and
+// E4M3 values are f16 values, and their product has at most 6 significant
+// bits and magnitude in [2^-10, 2688], so the f16 multiply does not round.
+BSQ_DEVICE void e2m1x8_scaled_f16x2(uint32_t w, uint32_t sf_byte, uint32_t (&h)[4])
+{
+    uint32_t s2;
+    asm("{\n\t.reg .b16 b;\n\tcvt.u16.u32 b, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}" : "=r"(s2) : "r"(sf_byte * 0x101u));
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[i]) : "r"(s2));
+}
+// d[j] = rn(rn(e2m1_j * sf) * t) for the eight codes of w (the inner product
+// is exact, see above).
+BSQ_DEVICE void e2m1x8_dequant(uint32_t w, uint32_t sf_byte, float t, float (&d)[8])
+{
+    uint32_t h[4];
+    e2m1x8_scaled_f16x2(w, sf_byte, h);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+        d[2 * i] = __fmul_rn(f.x, t);
+        d[2 * i + 1] = __fmul_rn(f.y, t);
+    }
+}
+
 // ---------------------------------------------------------------- E4M3
 // Four binary32 values -> four E4M3 bytes (element i in byte i), RNE satfinite.
 BSQ_DEVICE uint32_t e4m3x4(float v0, float v1, float v2, float v3)
@@ -120,6 +151,37 @@ BSQ_DEVICE uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
     return c;
 }
 
+// Philox4x32-10 with the round keys precomputed (k0 + r * 0x9E3779B9,
+// k1 + r * 0xBB67AE85 for round r), passed by value as a kernel parameter:
+// the same function as philox4x32_10, without the key schedule in the loop.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+inline PhiloxKeys philox_keys(uint64_t seed)
+{
+    PhiloxKeys k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r, a += 0x9E3779B9u, b += 0xBB67AE85u) {
+        k.k0[r] = a;
+        k.k1[r] = b;
+    }
+    return k;
+}
+BSQ_DEVICE uint4 philox4x32_10_keys(uint4 c, const PhiloxKeys& k)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x, p2 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p2 >> 32) ^ c.y ^ k.k0[r], (uint32_t)p2, (uint32_t)(p0 >> 32) ^ c.w ^ k.k1[r],
+                       (uint32_t)p0);
+    }
+    return c;
+}
+BSQ_DEVICE uint4 sr_block_bits_keys(const PhiloxKeys& k, uint32_t stream, uint64_t g)
+{
+    return philox4x32_10_keys(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, 0u), k);
+}
+
 // Random bits for 8 consecutive elements 8g .. 8g+7 of a stream: element
 // 8g + i takes the 16-bit half (i & 1) of word (i >> 1).
 BSQ_DEVICE uint4 sr_block_bits(uint64_t seed, uint32_t stream, uint64_t g)
@@ -135,55 +197,38 @@ BSQ_DEVICE uint32_t sr_pick16(uint4 w, int i)
 
 // ---------------------------------------------------------------- SR encoders
 // Stochastic rounding with 16 random bits r: with lo <= |v| < hi the two
-// neighbouring grid points, round up iff r < 65536 * (|v| - lo) / (hi - lo)
-// (exact in binary32: grid spacings are powers of two); |v| >= max saturates.
+// neighbouring grid points, round up iff r < 65536 * (|v| - lo) / (hi - lo);
+// |v| >= max saturates.  Where the grid spacing is the binary32 spacing of
+// |v| shifted by s bits (the normal ranges), (|v| - lo) / (hi - lo) * 65536
+// equals (the s dropped bits) / 2^(s-16), so "round up" is a carry out of
+// those bits after adding 2^s - 1 - (r << (s-16)); below the normal range the
+// comparison is made in binary32, where every step is exact.
 BSQ_DEVICE uint32_t e2m1_sr(float v, uint32_t r16)
 {
     const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
     const float a = fabsf(v);
-    if (a >= 6.0f) return sign | 7u;
-    float lo, inv_step;  // the spacing is a power of two, so * (1/spacing) is exact
-    uint32_t c;
-    if (a < 2.0f) {            // grid 0, .5, 1, 1.5 (spacing 0.5)
-        c = (uint32_t)__fmul_rn(a, 2.0f);      // floor(2a), exact for a < 2
-        lo = __fmul_rn((float)c, 0.5f);
-        inv_step = 2.0f;
-    } else if (a < 4.0f) {     // 2, 3 (spacing 1)
-        const uint32_t i = (uint32_t)a;       // 2 or 3
-        c = i + 2u;                           // codes 4, 5
-        lo = (float)i;
-        inv_step = 1.0f;
-    } else {                   // 4 .. 6 (spacing 2)
-        c = 6u;
-        lo = 4.0f;
-        inv_step = 0.5f;
+    // [1, 6): one mantissa bit kept (codes 2 .. 7 from the binary32 exponent and top bit)
+    uint32_t code = ((__float_as_uint(a) + (0x3FFFFFu - (r16 << 6))) >> 22) - 252u;
+    if (a < 1.0f) {  // grid 0, 0.5, 1 (codes 0, 1, 2)
+        const float y = __fmul_rn(a, 2.0f);
+        const float m = truncf(y);
+        code = (uint32_t)m + (((float)r16 < __fmul_rn(__fsub_rn(y, m), 65536.0f)) ? 1u : 0u);
     }
-    const float f = __fmul_rn(__fsub_rn(a, lo), inv_step);  // exact
-    if ((float)r16 < __fmul_rn(f, 65536.0f)) c += 1u;
-    return sign | c;
+    if (a >= 6.0f) code = 7u;
+    return sign | code;
 }
-
 BSQ_DEVICE uint32_t e4m3_sr(float v, uint32_t r16)
 {
     const uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
     const float a = fabsf(v);
-    if (a >= 448.0f) return sign | 0x7Eu;
-    const uint32_t ab = __float_as_uint(a);
-    float lo, inv_step;  // 1 / grid spacing, an exact power of two
-    uint32_t code;
-    if (a < 0.015625f) {       // subnormal range of E4M3: grid m * 2^-9
-        const uint32_t m = (uint32_t)__fmul_rn(a, 512.0f);   // floor, exact scaling
-        lo = __fmul_rn((float)m, 0.001953125f);
-        inv_step = 512.0f;
-        code = m;
-    } else {                   // normal: keep 3 mantissa bits
-        const uint32_t e = ab >> 23;                 // biased fp32 exponent (121..135)
-        lo = __uint_as_float(ab & 0xFFF00000u);
-        inv_step = __uint_as_float((257u - e) << 23); // 2^-(e-127-3)
-        code = ((e - 120u) << 3) | ((ab >> 20) & 7u);
+    // normal range [2^-6, 448): three mantissa bits kept; code = ((e - 120) << 3) | m
+    uint32_t code = ((__float_as_uint(a) + (0xFFFFFu - (r16 << 4))) >> 20) - 960u;
+    if (a < 0.015625f) {  // subnormal grid m * 2^-9
+        const float y = __fmul_rn(a, 512.0f);
+        const float m = truncf(y);
+        code = (uint32_t)m + (((float)r16 < __fmul_rn(__fsub_rn(y, m), 65536.0f)) ? 1u : 0u);
     }
-    const float f = __fmul_rn(__fsub_rn(a, lo), inv_step);
-    if ((float)r16 < __fmul_rn(f, 65536.0f)) code += 1u;   // carries into the exponent correctly
+    if (a >= 448.0f) code = 0x7Eu;
     return sign | code;
 }
 

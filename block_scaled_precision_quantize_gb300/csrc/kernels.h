@@ -15,9 +15,9 @@ void launch_group_finalize(float* scale, int64_t groups, cudaStream_t st);
 void launch_mxfp8_rowcol(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint8_t* rc, uint8_t* rs,
                          uint8_t* cc, uint8_t* cs, bool swz, cudaStream_t st);
 void launch_sf_pad_zero(uint8_t* sf, int64_t rows, int64_t cols, int sms, cudaStream_t st);
-void launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
-                    unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
-                    uint64_t seed, bool sr, bool swz, cudaStream_t st);
+cudaError_t launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
+                           unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
+                           uint64_t seed, bool sr, bool swz, cudaStream_t st);
 int64_t noalloc_requant_max_k();
 cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
                                    int64_t K, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,

@@ -314,62 +314,146 @@ __global__ void k_sf_pad_zero(uint8_t* __restrict__ sf, int64_t rows, int64_t co
 }
 
 // ---------------------------------------------------------------------------
-// Requant pass 1: per-column maximum of |D|, D = rn(rn(e2m1 * sf) * t), in
-// two deterministic stages.  Stage A: a thread owns 8 columns (one code word)
-// of a chunk of RQ_CHUNK rows and writes the chunk maxima to
-// part[chunk][K].  Stage B: one thread per column reduces over the chunks.
-constexpr int RQ_CHUNK = 32;
-constexpr int RQ_COLMAX_THREADS = 128;
+// Requant pass 1: per-column maximum of |D|, D = rn(rn(e2m1 * sf) * t), over
+// all rows.  CTA tile 128 rows x 256 columns, 256 threads: lane l of warp w
+// owns columns 32 (l & 7) .. +31 (one 16-byte code load per row) of rows
+// 4 w + (l >> 3) + 32 i (i = 0..3), all four loads in flight at once; the maxima are folded across the warp by shuffles and across the 8
+// warps in shared memory, and each column's maximum goes to colmax with one
+// unsigned atomicMax on the bits of a non-negative float (order-independent,
+// so the result is deterministic).  colmax must hold zeros beforehand.
+constexpr int RQ1_ROWS = 128, RQ1_COLS = 256;
+
+// The two SF bytes of columns c0 .. c0+31 (c0 a multiple of 32) of row r,
+// packed low = first.
+template <bool SWZ>
+BSQ_DEVICE uint32_t rq_sf_pair(const uint8_t* sf, int64_t r, int64_t c0, int64_t nsf)
+{
+    const int64_t b = c0 >> 4;
+    const int64_t o = SWZ ? sf_swizzled(r, b, (nsf + 3) >> 2) : r * nsf + b;
+    return (uint32_t)__ldg(sf + o) | ((uint32_t)__ldg(sf + o + 1) << 8);  // adjacent in both layouts
+}
 
 template <bool SWZ>
-__global__ void __launch_bounds__(RQ_COLMAX_THREADS) k_requant_colmax_part(const uint8_t* __restrict__ codes,
-                                                                           const uint8_t* __restrict__ sf,
-                                                                           const float* __restrict__ row_scale,
-                                                                           int64_t rows, int64_t K,
-                                                                           float* __restrict__ part)
+__global__ void __launch_bounds__(256) k_requant_colmax(const uint8_t* __restrict__ codes,
+                                                        const uint8_t* __restrict__ sf,
+                                                        const float* __restrict__ row_scale, int64_t rows, int64_t K,
+                                                        unsigned int* __restrict__ colmax)
 {
-    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // column group of 8
-    if (g >= (K >> 3)) return;
-    const int64_t r0 = (int64_t)blockIdx.y * RQ_CHUNK;
+    __shared__ float red[8][RQ1_COLS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t c0 = (int64_t)blockIdx.x * RQ1_COLS + 32 * (lane & 7);
+    const int64_t r0 = (int64_t)blockIdx.y * RQ1_ROWS + 4 * warp + (lane >> 3);
     const int64_t nsf = K >> 4;
-    float m[8];
+    float m[32];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = 0.0f;
-    const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes);
-#pragma unroll 8
-    for (int j = 0; j < RQ_CHUNK; ++j) {
-        const int64_t r = r0 + j;
-        if (r >= rows) break;
-        const uint32_t w = __ldg(cw + r * (K >> 3) + g);
-        const int64_t so = SWZ ? sf_swizzled(r, g >> 1, (nsf + 3) >> 2) : r * nsf + (g >> 1);
-        const float s = e4m3_to_f32(__ldg(sf + so));
-        const float t = __ldg(row_scale + r);
+    for (int i = 0; i < 32; ++i) m[i] = 0.0f;
+    if (c0 < K) {  // K % 16 == 0: a 32-column group is whole or half
+        const bool half = c0 + 16 >= K;
+        uint4 w[4];
+        uint32_t sp[4];
+        float t[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float a = e2m1_to_f32((w >> (4 * i)) & 7u);
-            m[i] = fmaxf(m[i], __fmul_rn(__fmul_rn(a, s), t));
+        for (int i = 0; i < 4; ++i) {
+            const int64_t r = r0 + 32 * i;
+            w[i] = make_uint4(0u, 0u, 0u, 0u);
+            sp[i] = 0u;
+            t[i] = 0.0f;
+            if (r < rows) {
+                const uint8_t* p = codes + r * (K >> 1) + (c0 >> 1);
+                if (!half) {
+                    if ((K & 31) == 0) {  // rows 16-byte aligned
+                        w[i] = __ldg(reinterpret_cast<const uint4*>(p));
+                    } else {              // rows 8-byte aligned
+                        const uint2 lo = __ldg(reinterpret_cast<const uint2*>(p));
+                        const uint2 hi = __ldg(reinterpret_cast<const uint2*>(p) + 1);
+                        w[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    }
+                    sp[i] = rq_sf_pair<SWZ>(sf, r, c0, nsf);
+                } else {
+                    const uint2 h = __ldg(reinterpret_cast<const uint2*>(p));
+                    w[i] = make_uint4(h.x, h.y, 0u, 0u);
+                    const int64_t o = SWZ ? sf_swizzled(r, c0 >> 4, (nsf + 3) >> 2) : r * nsf + (c0 >> 4);
+                    sp[i] = __ldg(sf + o);
+                }
+                t[i] = __ldg(row_scale + r);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ww[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float d[8];
+                e2m1x8_dequant(ww[q], (sp[i] >> (8 * (q >> 1))) & 0xFFu, t[i], d);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) m[8 * q + j] = fmaxf(m[8 * q + j], fabsf(d[j]));
+            }
         }
     }
-    float4* dst = reinterpret_cast<float4*>(part + (int64_t)blockIdx.y * K + 8 * g);
-    dst[0] = make_float4(m[0], m[1], m[2], m[3]);
-    dst[1] = make_float4(m[4], m[5], m[6], m[7]);
+    // fold the four row lanes (l >> 3) of each column group, then the warps
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], 8));
+        m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], 16));
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) red[warp][32 * lane + i] = m[i];
+    }
+    __syncthreads();
+    const int64_t c = (int64_t)blockIdx.x * RQ1_COLS + threadIdx.x;
+    float v = red[0][threadIdx.x];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) v = fmaxf(v, red[w][threadIdx.x]);
+    if (c < K && v > 0.0f) atomicMax(colmax + c, __float_as_uint(v));
 }
 
-__global__ void __launch_bounds__(256) k_requant_colmax_reduce(const float* __restrict__ part, int64_t nchunks,
-                                                               int64_t K, unsigned int* __restrict__ colmax)
+// Requant pass 2.  CTA tile: 256 source rows (m) x 64 source columns (k),
+// 256 threads.  The tile is dequantized into shared memory transposed,
+// DT[k][m] in binary32: thread m dequantizes source row m (two 16-byte code
+// loads, its four SF bytes and its row scale, all issued up front) and
+// writes column m of DT.  The 4-float chunk c = m >> 2 of a row is stored at
+// chunk c ^ ((c >> 3) & 3), which keeps the 16-byte reads of each
+// quarter-warp below on distinct banks.  Then each half-warp produces one
+// output row k (a source column) per step, warp w taking rows 16 i + 2 w + h:
+// lane l (l16 = l & 15) owns m = 16 l16 .. +15, i.e. one whole NVFP4 block
+// and half of one MXFP8 block (block maximum with its neighbour lane), two
+// Philox calls per format for its 16 random 16-bit draws, and writes 16 + 8
+// contiguous code bytes: each half-warp store covers 256 + 128 contiguous
+// bytes of one output row.  The NVFP4 per-row scales of the tile's rows are
+// computed once per CTA into shared memory.
+constexpr int RQ_TM = 256, RQ_TK = 64;
+
+BSQ_DEVICE int rq_phys(int k, int m)
 {
-    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= K) return;
-    float m = 0.0f;
-    for (int64_t j = 0; j < nchunks; ++j) m = fmaxf(m, __ldg(part + j * K + c));
-    colmax[c] = __float_as_uint(m);
+    const int c = m >> 2;
+    return k * RQ_TM + 4 * (c ^ ((c >> 3) & 3)) + (m & 3);
 }
 
-// Requant pass 2.  CTA tile: 128 source rows (m) x 64 source columns (k),
-// 256 threads.  The tile is dequantized into shared memory (binary32), then
-// each thread produces one 32-element run of one output row (a source
-// column): the MXFP8 block and two NVFP4 blocks, with RNE or Philox SR.
-constexpr int RQ_TM = 128, RQ_TK = 64;
+// Scale factors of output row k: lane l16 (0..15) of a half-warp holds block
+// col0 + l16 / step of the row (col0 a multiple of 4).  Four consecutive
+// blocks share one 32-bit word when the swizzled layout is used (its column
+// padding absorbs a short last group) or the row length is a multiple of 4;
+// otherwise each block is stored as a byte.  Blocks at or past ncols are not
+// stored.  All 32 lanes must call this (the gathers are warp shuffles; they
+// stay inside each half-warp for the writing lanes).
+BSQ_DEVICE void rq_store_sf(uint8_t* sf, bool swz, int64_t k, int64_t col0, int64_t ncols, uint32_t v, int l16,
+                            int step)
+{
+    const int64_t col = col0 + l16 / step;
+    if (swz || (ncols & 3) == 0) {
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, v, step);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, v, 2 * step);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, v, 3 * step);
+        if ((l16 & (4 * step - 1)) == 0 && col < ncols) {
+            const uint32_t word = (v & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) | ((b3 & 0xFFu) << 24);
+            const int64_t off = swz ? sf_swizzled(k, col, (ncols + 3) >> 2) : k * ncols + col;
+            *reinterpret_cast<uint32_t*>(sf + off) = word;
+        }
+    } else if ((l16 & (step - 1)) == 0 && col < ncols) {
+        sf[k * ncols + col] = (uint8_t)v;
+    }
+}
 
 template <bool SWZ, bool SR, bool NV, bool MX>
 __global__ void __launch_bounds__(256) k_requant_main(const uint8_t* __restrict__ codes,
@@ -378,111 +462,136 @@ __global__ void __launch_bounds__(256) k_requant_main(const uint8_t* __restrict_
                                                       const unsigned int* __restrict__ colmax,
                                                       uint8_t* __restrict__ nv_codes, uint8_t* __restrict__ nv_sf,
                                                       float* __restrict__ nv_scale, uint8_t* __restrict__ mx_codes,
-                                                      uint8_t* __restrict__ mx_sf, uint64_t seed)
+                                                      uint8_t* __restrict__ mx_sf, const PhiloxKeys keys)
 {
-    __shared__ __align__(16) float D[RQ_TM * RQ_TK];
-    const int tid = threadIdx.x;
+    extern __shared__ __align__(16) float DT[];  // [RQ_TK][RQ_TM]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t m0 = (int64_t)blockIdx.y * RQ_TM, k0 = (int64_t)blockIdx.x * RQ_TK;
     const int64_t nsf_in = K >> 4;
-    const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int item = tid + 256 * i;
-        const int m = item >> 3, g = item & 7;
-        const int64_t gm = m0 + m, gk = k0 + 8 * g;
-        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-        if (gm < rows && gk < K) {
-            const uint32_t w = __ldg(cw + gm * (K >> 3) + (gk >> 3));
-            const int64_t so = SWZ ? sf_swizzled(gm, gk >> 4, (nsf_in + 3) >> 2) : gm * nsf_in + (gk >> 4);
-            const float s = e4m3_to_f32(__ldg(sf + so));
-            const float t = __ldg(row_scale + gm);
-            float d[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) d[j] = __fmul_rn(__fmul_rn(e2m1_to_f32((w >> (4 * j)) & 0xFu), s), t);
-            lo = make_float4(d[0], d[1], d[2], d[3]);
-            hi = make_float4(d[4], d[5], d[6], d[7]);
-        }
-        float4* dst = reinterpret_cast<float4*>(D + m * RQ_TK + 8 * g);
-        dst[0] = lo;
-        dst[1] = hi;
-    }
-    __syncthreads();
-    const int c = tid & 63, mb = tid >> 6;
-    const int64_t gk = k0 + c, gm = m0 + 32 * mb;
-    if (gk >= K || gm >= rows) return;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = D[(32 * mb + i) * RQ_TK + c];
-    const uint64_t idx0 = (uint64_t)gk * (uint64_t)rows + (uint64_t)gm;  // index in Y of v[0]
-    if (MX) {
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    {
+        // dequantize source row m = tid, columns k0 .. k0+63 (K % 16 == 0)
+        const int m = tid;
+        const int64_t gm = m0 + m;
         uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        uint32_t s = 0;
-        if (amax > 0.f) {
-            const int X = mx_exponent(__float_as_uint(amax));
-            const float mul = mx_multiplier(X);
-            s = (uint32_t)(X + 127);
-            if (SR) {
+        uint32_t sfw = 0u;
+        float t = 0.0f;
+        const int64_t nw_all = (K - k0) >> 3;
+        const int nw = nw_all < 8 ? (int)nw_all : 8;  // code words of 8 columns in range
+        if (gm < rows) {
+            const uint8_t* p = codes + gm * (K >> 1) + (k0 >> 1);
+            if (nw == 8 && (K & 31) == 0) {  // rows 16-byte aligned
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+                const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            } else if (nw == 8) {            // rows 8-byte aligned
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 rb = sr_block_bits(seed, 1u, (idx0 >> 3) + q);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t code = e4m3_sr(__fmul_rn(v[8 * q + j], mul), sr_pick16(rb, j));
-                        w[2 * q + (j >> 2)] |= code << (8 * (j & 3));
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const uint2 h = __ldg(reinterpret_cast<const uint2*>(p) + i);
+                    w[2 * i] = h.x;
+                    w[2 * i + 1] = h.y;
                 }
             } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    w[j] = e4m3x4(__fmul_rn(v[4 * j], mul), __fmul_rn(v[4 * j + 1], mul),
-                                  __fmul_rn(v[4 * j + 2], mul), __fmul_rn(v[4 * j + 3], mul));
+                for (int i = 0; i < nw; ++i) w[i] = __ldg(reinterpret_cast<const uint32_t*>(p) + i);
             }
+            const int64_t b0 = k0 >> 4;  // first SF column (a multiple of 4)
+            const int64_t o = SWZ ? sf_swizzled(gm, b0, (nsf_in + 3) >> 2) : gm * nsf_in + b0;
+            if (nw == 8 && (SWZ || (nsf_in & 3) == 0)) {
+                sfw = __ldg(reinterpret_cast<const uint32_t*>(sf + o));
+            } else {
+                for (int i = 0; i < (nw + 1) / 2; ++i) sfw |= (uint32_t)__ldg(sf + o + i) << (8 * i);
+            }
+            t = __ldg(row_scale + gm);
         }
-        uint4* dst = reinterpret_cast<uint4*>(mx_codes + gk * rows + gm);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        store_sf(mx_sf, SWZ, gk, gm >> 5, rows >> 5, s);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float d[8];
+            e2m1x8_dequant(w[q], (sfw >> (8 * (q >> 1))) & 0xFFu, t, d);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) DT[rq_phys(8 * q + j, m)] = d[j];
+        }
     }
-    if (NV) {
-        const float t = __fdiv_rn(__uint_as_float(__ldg(colmax + gk)), kNvfp4ScaleDivisor);
-        if (blockIdx.y == 0 && mb == 0) nv_scale[gk] = t;
-        const float six_t = __fmul_rn(6.0f, t);
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        uint32_t sfb[2] = {0u, 0u};
-        if (t != 0.0f) {
+    __shared__ float tq[RQ_TK];  // NVFP4 per-row scales of the tile's output rows
+    if (NV && tid < RQ_TK) {
+        const int64_t gk = k0 + tid;
+        float t = 0.0f;
+        if (gk < K) {
+            t = __fdiv_rn(__uint_as_float(__ldg(colmax + gk)), kNvfp4ScaleDivisor);
+            if (blockIdx.y == 0) nv_scale[gk] = t;
+        }
+        tq[tid] = t;
+    }
+    __syncthreads();
+    const int l16 = lane & 15, half = lane >> 4;
+    const int64_t gm = m0 + 16 * l16;   // first source row of this lane
+    const bool valid = gm < rows;        // rows % 32 == 0: whole MXFP8 blocks drop out
+    for (int it = 0; it < RQ_TK / 16; ++it) {
+        const int kk = 16 * it + 2 * warp + half;
+        const int64_t gk = k0 + kk;
+        if (k0 + 16 * it >= K) break;   // K % 16 == 0: the 16 rows of a step are all in or all out
+        float v[16];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float* xb = v + 16 * h;
-                float ab = 0.f;
+        for (int j = 0; j < 4; ++j) {
+            const float4 a = *reinterpret_cast<const float4*>(DT + rq_phys(kk, 16 * l16 + 4 * j));
+            v[4 * j] = a.x; v[4 * j + 1] = a.y; v[4 * j + 2] = a.z; v[4 * j + 3] = a.w;
+        }
+        float am = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(xb[i]));
-                const BlockScale bs = nvfp4_block_scale(ab, six_t, t);
-                sfb[h] = bs.sf;
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
+        const uint64_t g8 = ((uint64_t)gk * (uint64_t)rows + (uint64_t)gm) >> 3;  // Philox counter of v[0..7]
+        if (MX) {
+            const float ab = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));  // MXFP8 block (32 rows)
+            uint32_t w[4] = {0u, 0u, 0u, 0u}, sc = 0u;
+            if (ab > 0.0f) {
+                const int X = mx_exponent(__float_as_uint(ab));
+                const float mul = mx_multiplier(X);
+                sc = (uint32_t)(X + 127);
                 if (SR) {
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const uint4 rb = sr_block_bits(seed, 0u, (idx0 >> 3) + 2 * h + q);
-                        uint32_t word = 0;
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 rb = sr_block_bits_keys(keys, 1u, g8 + h);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            word |= e2m1_sr(__fmul_rn(xb[8 * q + j], bs.enc), sr_pick16(rb, j)) << (4 * j);
-                        w[2 * h + q] = word;
+                            w[2 * h + (j >> 2)] |= e4m3_sr(__fmul_rn(v[8 * h + j], mul), sr_pick16(rb, j)) << (8 * (j & 3));
                     }
                 } else {
-                    const uint2 cc = encode16(xb, bs.enc);
-                    w[2 * h] = cc.x;
-                    w[2 * h + 1] = cc.y;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        w[q] = e4m3x4(__fmul_rn(v[4 * q], mul), __fmul_rn(v[4 * q + 1], mul), __fmul_rn(v[4 * q + 2], mul),
+                                      __fmul_rn(v[4 * q + 3], mul));
                 }
             }
+            if (valid) *reinterpret_cast<uint4*>(mx_codes + gk * rows + gm) = make_uint4(w[0], w[1], w[2], w[3]);
+            rq_store_sf(mx_sf, SWZ, gk, m0 >> 5, rows >> 5, sc, l16, 2);
         }
-        *reinterpret_cast<uint4*>(nv_codes + gk * (rows >> 1) + (gm >> 1)) = make_uint4(w[0], w[1], w[2], w[3]);
-        store_sf(nv_sf, SWZ, gk, gm >> 4, rows >> 4, sfb[0]);
-        store_sf(nv_sf, SWZ, gk, (gm >> 4) + 1, rows >> 4, sfb[1]);
+        if (NV) {
+            const float t = tq[kk];
+            uint32_t w[2] = {0u, 0u}, sfb = 0u;
+            if (t != 0.0f) {
+                const BlockScale bs = nvfp4_block_scale(am, __fmul_rn(6.0f, t), t);
+                sfb = bs.sf;
+                if (SR) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 rb = sr_block_bits_keys(keys, 0u, g8 + h);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) w[h] |= e2m1_sr(__fmul_rn(v[8 * h + j], bs.enc), sr_pick16(rb, j)) << (4 * j);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        w[h] = e2m1x8(__fmul_rn(v[8 * h], bs.enc), __fmul_rn(v[8 * h + 1], bs.enc),
+                                      __fmul_rn(v[8 * h + 2], bs.enc), __fmul_rn(v[8 * h + 3], bs.enc),
+                                      __fmul_rn(v[8 * h + 4], bs.enc), __fmul_rn(v[8 * h + 5], bs.enc),
+                                      __fmul_rn(v[8 * h + 6], bs.enc), __fmul_rn(v[8 * h + 7], bs.enc));
+                }
+            }
+            if (valid) *reinterpret_cast<uint2*>(nv_codes + gk * (rows >> 1) + (gm >> 1)) = make_uint2(w[0], w[1]);
+            rq_store_sf(nv_sf, SWZ, gk, m0 >> 4, rows >> 4, sfb, l16, 1);
+        }
     }
 }
+constexpr size_t RQ_SMEM = (size_t)RQ_TM * RQ_TK * sizeof(float);  // 64 KB
 
 // ---------------------------------------------------------------------------
 // Helpers.
@@ -604,37 +713,52 @@ void launch_sf_pad_zero(uint8_t* sf, int64_t rows, int64_t cols, int sms, cudaSt
     k_sf_pad_zero<<<sms * 4, 256, 0, st>>>(sf, rows, cols);
 }
 
-void launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
-                    unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
-                    uint64_t seed, bool sr, bool swz, cudaStream_t st)
+// Both requant passes; colmax (K words) is cleared here when NVFP4 output is wanted.
+template <bool S, bool R, bool N, bool M>
+static cudaError_t requant_main(dim3 grid, const uint8_t* codes, const uint8_t* sf, const float* row_scale,
+                                int64_t rows, int64_t K, const unsigned int* colmax, uint8_t* nvc, uint8_t* nvs,
+                                float* nvt, uint8_t* mxc, uint8_t* mxs, uint64_t seed, cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(k_requant_main<S, R, N, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)RQ_SMEM);
+        if (err != cudaSuccess) return err;
+        attr_set = true;
+    }
+    k_requant_main<S, R, N, M><<<grid, 256, RQ_SMEM, st>>>(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc,
+                                                            mxs, philox_keys(seed));
+    return cudaGetLastError();
+}
+
+static cudaError_t requant_passes(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
+                                  int64_t K, unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc,
+                                  uint8_t* mxs, uint64_t seed, bool sr, bool swz, cudaStream_t st)
 {
     const bool nv = nvc != nullptr, mx = mxc != nullptr;
     if (nv) {
-        // workspace: colmax [K] then the per-chunk maxima [nchunks][K]
-        const int64_t nchunks = (rows + RQ_CHUNK - 1) / RQ_CHUNK;
-        float* part = reinterpret_cast<float*>(colmax) + ((K + 63) & ~(int64_t)63);
-        dim3 g1((unsigned)(((K >> 3) + RQ_COLMAX_THREADS - 1) / RQ_COLMAX_THREADS), (unsigned)nchunks);
-        if (swz) k_requant_colmax_part<true><<<g1, RQ_COLMAX_THREADS, 0, st>>>(codes, sf, row_scale, rows, K, part);
-        else k_requant_colmax_part<false><<<g1, RQ_COLMAX_THREADS, 0, st>>>(codes, sf, row_scale, rows, K, part);
-        k_requant_colmax_reduce<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(part, nchunks, K, colmax);
+        cudaError_t err = cudaMemsetAsync(colmax, 0, (size_t)K * sizeof(unsigned int), st);
+        if (err != cudaSuccess) return err;
+        dim3 g1((unsigned)((K + RQ1_COLS - 1) / RQ1_COLS), (unsigned)((rows + RQ1_ROWS - 1) / RQ1_ROWS));
+        if (swz) k_requant_colmax<true><<<g1, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
+        else k_requant_colmax<false><<<g1, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
     }
     dim3 g2((unsigned)((K + RQ_TK - 1) / RQ_TK), (unsigned)((rows + RQ_TM - 1) / RQ_TM));
-#define BSQ_RQ(S, R, N, M)                                                                                   \
-    k_requant_main<S, R, N, M><<<g2, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, \
-                                                   seed)
-#define BSQ_RQ2(S, R)                          \
-    do {                                       \
-        if (nv && mx) BSQ_RQ(S, R, true, true); \
-        else if (nv) BSQ_RQ(S, R, true, false); \
-        else BSQ_RQ(S, R, false, true);        \
-    } while (0)
-    if (swz) {
-        if (sr) BSQ_RQ2(true, true); else BSQ_RQ2(true, false);
-    } else {
-        if (sr) BSQ_RQ2(false, true); else BSQ_RQ2(false, false);
-    }
+#define BSQ_RQ(S, R, N, M) \
+    requant_main<S, R, N, M>(g2, codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, st)
+#define BSQ_RQ2(S, R)                                                                                 \
+    (nv && mx ? BSQ_RQ(S, R, true, true) : nv ? BSQ_RQ(S, R, true, false) : BSQ_RQ(S, R, false, true))
+    if (swz) return sr ? BSQ_RQ2(true, true) : BSQ_RQ2(true, false);
+    return sr ? BSQ_RQ2(false, true) : BSQ_RQ2(false, false);
 #undef BSQ_RQ2
 #undef BSQ_RQ
+}
+
+cudaError_t launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
+                           unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
+                           uint64_t seed, bool sr, bool swz, cudaStream_t st)
+{
+    return requant_passes(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, sr, swz, st);
 }
 
 void launch_sf_swizzle(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, int dir, int sms,
@@ -669,41 +793,7 @@ void launch_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t
 namespace {
 
 constexpr int64_t kNoallocMaxK = 65536;
-constexpr int kNoallocRows = 64;  // rows per CTA of the column-maximum pass
 __device__ __align__(256) unsigned int g_requant_colmax[kNoallocMaxK];
-
-// Column maxima of |D| straight into the shared array: a thread owns 8
-// columns of kNoallocRows rows and folds them in with unsigned atomicMax on
-// the bits of non-negative floats (order-independent, so deterministic).
-template <bool SWZ>
-__global__ void __launch_bounds__(128) k_requant_colmax_atomic(const uint8_t* __restrict__ codes,
-                                                               const uint8_t* __restrict__ sf,
-                                                               const float* __restrict__ row_scale, int64_t rows,
-                                                               int64_t K, unsigned int* __restrict__ colmax)
-{
-    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= (K >> 3)) return;
-    const int64_t r0 = (int64_t)blockIdx.y * kNoallocRows;
-    const int64_t nsf = K >> 4;
-    float m[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = 0.0f;
-    const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes);
-#pragma unroll 8
-    for (int j = 0; j < kNoallocRows; ++j) {
-        const int64_t r = r0 + j;
-        if (r >= rows) break;
-        const uint32_t w = __ldg(cw + r * (K >> 3) + g);
-        const int64_t so = SWZ ? sf_swizzled(r, g >> 1, (nsf + 3) >> 2) : r * nsf + (g >> 1);
-        const float s = e4m3_to_f32(__ldg(sf + so));
-        const float t = __ldg(row_scale + r);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], __fmul_rn(__fmul_rn(e2m1_to_f32((w >> (4 * i)) & 7u), s), t));
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        if (m[i] > 0.0f) atomicMax(colmax + 8 * g + i, __float_as_uint(m[i]));
-}
 
 // Device address of g_requant_colmax, looked up once per device with that
 // device current (the host-side name is only a stand-in for it).
@@ -739,32 +829,7 @@ cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, cons
     unsigned int* colmax = nullptr;
     cudaError_t err = noalloc_scratch(&colmax);
     if (err != cudaSuccess) return err;
-    const bool nv = nvc != nullptr, mx = mxc != nullptr;
-    if (nv) {
-        err = cudaMemsetAsync(colmax, 0, (size_t)K * sizeof(unsigned int), st);
-        if (err != cudaSuccess) return err;
-        dim3 g1((unsigned)(((K >> 3) + 127) / 128), (unsigned)((rows + kNoallocRows - 1) / kNoallocRows));
-        if (swz) k_requant_colmax_atomic<true><<<g1, 128, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
-        else k_requant_colmax_atomic<false><<<g1, 128, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
-    }
-    dim3 g2((unsigned)((K + RQ_TK - 1) / RQ_TK), (unsigned)((rows + RQ_TM - 1) / RQ_TM));
-#define BSQ_RQN(S, R, N, M)                                                                                   \
-    k_requant_main<S, R, N, M><<<g2, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, \
-                                                   seed)
-#define BSQ_RQN2(S, R)                            \
-    do {                                          \
-        if (nv && mx) BSQ_RQN(S, R, true, true);  \
-        else if (nv) BSQ_RQN(S, R, true, false);  \
-        else BSQ_RQN(S, R, false, true);          \
-    } while (0)
-    if (swz) {
-        if (sr) BSQ_RQN2(true, true); else BSQ_RQN2(true, false);
-    } else {
-        if (sr) BSQ_RQN2(false, true); else BSQ_RQN2(false, false);
-    }
-#undef BSQ_RQN2
-#undef BSQ_RQN
-    return cudaGetLastError();
+    return requant_passes(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, sr, swz, st);
 }
 
 }  // namespace bsq

@@ -165,10 +165,10 @@ bsq_status quantize_mxfp8_rowcol(const void* x, int64_t rows, int64_t K, int64_t
  *   mx_*                   out MXFP8 of Y: codes [K][rows], sf [K][rows/32]
  *                          (both NULL: skip)
  *   workspace              device scratch of bsq_requant_workspace_size()
- *                          bytes (column maxima of |D| and their per-32-row
- *                          partial maxima); may be NULL when that
- *                          size is 0
- * rows % 32 == 0, K % 16 == 0.
+ *                          bytes (the column maxima of |D|); may be NULL
+ *                          when that size is 0
+ * rows % 32 == 0, K % 16 == 0; codes and the output codes 16-byte aligned,
+ * the SF buffers (input and outputs) 4-byte aligned (else BSQ_ERR_ALIGN).
  * ------------------------------------------------------------------------- */
 size_t bsq_requant_workspace_size(int64_t rows, int64_t K, int32_t nvfp4_target);
 bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const float* row_scale,

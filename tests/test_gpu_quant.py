@@ -110,7 +110,7 @@ def _requant_inputs(O, rows, K, seed):
     return O.nvfp4_quantize_rows(x)
 
 
-@pytest.mark.parametrize("rows,K", [(64, 96), (160, 2048), (1024, 768), (32, 16)])
+@pytest.mark.parametrize("rows,K", [(64, 96), (160, 2048), (1024, 768), (32, 16), (64, 48), (96, 80), (288, 176)])
 @pytest.mark.parametrize("sr", [False, True])
 @pytest.mark.parametrize("swz", [False, True])
 def test_requant_transpose(gpu, O, rows, K, sr, swz):
