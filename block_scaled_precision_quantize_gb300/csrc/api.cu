@@ -144,6 +144,7 @@ bsq_status quantize_mxfp8_rowcol(const void* x, int64_t rows, int64_t K, int64_t
     if ((row_codes && !row_sf) || (col_codes && !col_sf)) return BSQ_ERR_NULL;
     if (!a16(x) || ldx % 8 != 0 || (row_codes && !a16(row_codes)) || (col_codes && !a16(col_codes)))
         return BSQ_ERR_ALIGN;
+    if ((row_codes && !a4(row_sf)) || (col_codes && !a4(col_sf))) return BSQ_ERR_ALIGN;
     int sms;
     bsq_status st = current_device(&sms);
     if (st != BSQ_OK) return st;

@@ -218,11 +218,40 @@ __global__ void k_group_finalize(float* __restrict__ scale, int64_t groups)
 
 // ---------------------------------------------------------------------------
 // MXFP8 row + column copies.  CTA tile 128 rows x 128 columns, 512 threads.
-// Row copy straight from registers (4 lanes per 32-element block); the tile is
-// staged in shared memory (rows padded by 16 bytes) for the column copy, where
-// a warp reads 32 adjacent columns of one row per step.
+// Phase 1 (row copy): thread item = (row r, 16-byte chunk ch of 8 bf16), four
+// lanes per 32-element block, straight from registers; the tile also goes to
+// shared memory (256-byte rows, chunk ch of row r stored at ch ^ ((r >> 4) & 7)).
+// Phase 2 (column copy): thread = (column pair p, row group g): it reads
+// 16 bf16 pairs (columns 2p, 2p+1, rows 16g .. +15), one 32-bit word each; the
+// chunk permutation puts the 8 row groups of a warp on distinct banks.  An
+// MXFP8 block of a column (32 rows) is two row groups (block maximum with the
+// lane 4 away); each thread writes 16 contiguous bytes per column, so the 8
+// row groups of a column store 128 contiguous bytes.  The block scale bytes of
+// a row (phase 1) or of a column (phase 2) are gathered by shuffles into one
+// 32-bit store of 4 consecutive blocks where the layout allows it.
 constexpr int MX_TILE = 128;
-constexpr int MX_LD = MX_TILE + 8;  // bf16 elements per staged row
+
+BSQ_DEVICE int mx_chunk(int r, int ch) { return r * 16 + (ch ^ ((r >> 4) & 7)); }  // in 16-byte units
+
+// Block scale byte v of block `col` of SF row `row`; lanes `lane0`, lane0 +
+// stride, +2 stride, +3 stride hold blocks col0 .. col0+3 (col0 % 4 == 0).
+// All lanes call; the lane with `leader` set writes.
+BSQ_DEVICE void mx_store_sf4(uint8_t* sf, bool swz, int64_t row, int64_t col0, int64_t ncols, uint32_t v,
+                             int stride, bool leader, bool in_range)
+{
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, v, stride);
+    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, v, 2 * stride);
+    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, v, 3 * stride);
+    if (!leader || !in_range) return;
+    const uint32_t b[4] = {v & 0xFFu, b1 & 0xFFu, b2 & 0xFFu, b3 & 0xFFu};
+    if (swz || ((ncols & 3) == 0 && col0 + 4 <= ncols)) {
+        const int64_t off = swz ? sf_swizzled(row, col0, (ncols + 3) >> 2) : row * ncols + col0;
+        *reinterpret_cast<uint32_t*>(sf + off) = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+    } else {
+        for (int j = 0; j < 4; ++j)
+            if (col0 + j < ncols) sf[row * ncols + col0 + j] = (uint8_t)b[j];
+    }
+}
 
 template <bool SWZ, bool ROW, bool COL>
 __global__ void __launch_bounds__(512) k_mxfp8_rowcol(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
@@ -230,75 +259,100 @@ __global__ void __launch_bounds__(512) k_mxfp8_rowcol(const uint16_t* __restrict
                                                       uint8_t* __restrict__ row_sf, uint8_t* __restrict__ col_codes,
                                                       uint8_t* __restrict__ col_sf)
 {
-    __shared__ __align__(16) uint16_t tile[MX_TILE * MX_LD];
-    const int tid = threadIdx.x;
+    __shared__ __align__(16) uint4 tile[MX_TILE * 16];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row0 = (int64_t)blockIdx.y * MX_TILE, col0 = (int64_t)blockIdx.x * MX_TILE;
     const int64_t nsf_row = K >> 5, nsf_col = rows >> 5;
+    uint4 v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int item = tid + 512 * i;
         const int r = item >> 4, ch = item & 15;
         const int64_t gr = row0 + r, gc = col0 + 8 * ch;
-        const bool ok = gr < rows && gc < K;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (ok) v = ldg_stream(x + gr * ldx + gc);
-        if (COL) *reinterpret_cast<uint4*>(tile + r * MX_LD + 8 * ch) = v;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (gr < rows && gc < K) v[i] = ldg_stream(x + gr * ldx + gc);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int item = tid + 512 * i;
+        const int r = item >> 4, ch = item & 15;
+        const int64_t gr = row0 + r, gc = col0 + 8 * ch;
+        if (COL) tile[mx_chunk(r, ch)] = v[i];
         if (ROW) {
-            uint32_t m = absmax_bf16x2(0u, v.x);
-            m = absmax_bf16x2(m, v.y);
-            m = absmax_bf16x2(m, v.z);
-            m = absmax_bf16x2(m, v.w);
+            uint32_t m = absmax_bf16x2(0u, v[i].x);
+            m = absmax_bf16x2(m, v[i].y);
+            m = absmax_bf16x2(m, v[i].z);
+            m = absmax_bf16x2(m, v[i].w);
             m = fold_halves(m);
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            if (ok) {
-                uint2 c = make_uint2(0u, 0u);
-                uint32_t s = 0;
-                if (m) {
-                    const int X = mx_exponent(m << 16);
-                    const float mul = mx_multiplier(X);
-                    s = (uint32_t)(X + 127);
-                    c.x = e4m3x4(__fmul_rn(bf16_lo(v.x), mul), __fmul_rn(bf16_hi(v.x), mul),
-                                 __fmul_rn(bf16_lo(v.y), mul), __fmul_rn(bf16_hi(v.y), mul));
-                    c.y = e4m3x4(__fmul_rn(bf16_lo(v.z), mul), __fmul_rn(bf16_hi(v.z), mul),
-                                 __fmul_rn(bf16_lo(v.w), mul), __fmul_rn(bf16_hi(v.w), mul));
-                }
-                *reinterpret_cast<uint2*>(row_codes + gr * K + gc) = c;
-                if ((ch & 3) == 0) store_sf(row_sf, SWZ, gr, gc >> 5, nsf_row, s);
+            uint2 c = make_uint2(0u, 0u);
+            uint32_t s = 0;
+            if (m) {
+                const int X = mx_exponent(m << 16);
+                const float mul = mx_multiplier(X);
+                s = (uint32_t)(X + 127);
+                c.x = e4m3x4(__fmul_rn(bf16_lo(v[i].x), mul), __fmul_rn(bf16_hi(v[i].x), mul),
+                             __fmul_rn(bf16_lo(v[i].y), mul), __fmul_rn(bf16_hi(v[i].y), mul));
+                c.y = e4m3x4(__fmul_rn(bf16_lo(v[i].z), mul), __fmul_rn(bf16_hi(v[i].z), mul),
+                             __fmul_rn(bf16_lo(v[i].w), mul), __fmul_rn(bf16_hi(v[i].w), mul));
             }
+            const bool ok = gr < rows && gc < K;
+            if (ok) *reinterpret_cast<uint2*>(row_codes + gr * K + gc) = c;
+            // blocks of this row: chunk leaders ch = 0, 4, 8, 12 (lanes 4 apart)
+            mx_store_sf4(row_sf, SWZ, gr, col0 >> 5, nsf_row, s, 4, (ch & 15) == 0, gr < rows && col0 < K);
         }
     }
     if (!COL) return;
     __syncthreads();
-    const int c = tid & 127, rb = tid >> 7;
-    const int64_t gc = col0 + c, gr = row0 + 32 * rb;
-    if (gc >= K || gr >= rows) return;
-    float v[32];
-    uint32_t m = 0;
+    const int p = (lane & 3) + 4 * warp;  // column pair: columns 2p, 2p+1 of the tile
+    const int g = lane >> 2;              // row group: rows 16g .. 16g+15
+    const int64_t gc = col0 + 2 * p, gr = row0 + 16 * g;
+    float a[16], b[16];
+    uint32_t ma = 0, mb = 0;
+    const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint32_t b = tile[(32 * rb + i) * MX_LD + c];
-        m = max(m, b & 0x7FFFu);
-        v[i] = __uint_as_float(b << 16);
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * g + i;
+        const uint32_t w = tw[4 * mx_chunk(r, p >> 2) + (p & 3)];
+        ma = max(ma, w & 0x7FFFu);
+        mb = max(mb, (w >> 16) & 0x7FFFu);
+        a[i] = __uint_as_float(w << 16);
+        b[i] = __uint_as_float(w & 0xFFFF0000u);
     }
-    uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-    uint32_t s = 0;
-    if (m) {
-        const int X = mx_exponent(m << 16);
+    ma = max(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 4));  // the other half of the 32-row block
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 4));
+    uint32_t sa = 0, sb = 0;
+    uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
+    if (ma) {
+        const int X = mx_exponent(ma << 16);
         const float mul = mx_multiplier(X);
-        s = (uint32_t)(X + 127);
-        uint32_t w[8];
+        sa = (uint32_t)(X + 127);
+        uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            w[j] = e4m3x4(__fmul_rn(v[4 * j], mul), __fmul_rn(v[4 * j + 1], mul), __fmul_rn(v[4 * j + 2], mul),
-                          __fmul_rn(v[4 * j + 3], mul));
-        o0 = make_uint4(w[0], w[1], w[2], w[3]);
-        o1 = make_uint4(w[4], w[5], w[6], w[7]);
+        for (int j = 0; j < 4; ++j)
+            w[j] = e4m3x4(__fmul_rn(a[4 * j], mul), __fmul_rn(a[4 * j + 1], mul), __fmul_rn(a[4 * j + 2], mul),
+                          __fmul_rn(a[4 * j + 3], mul));
+        oa = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(col_codes + gc * rows + gr);
-    dst[0] = o0;
-    dst[1] = o1;
-    store_sf(col_sf, SWZ, gc, gr >> 5, nsf_col, s);
+    if (mb) {
+        const int X = mx_exponent(mb << 16);
+        const float mul = mx_multiplier(X);
+        sb = (uint32_t)(X + 127);
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = e4m3x4(__fmul_rn(b[4 * j], mul), __fmul_rn(b[4 * j + 1], mul), __fmul_rn(b[4 * j + 2], mul),
+                          __fmul_rn(b[4 * j + 3], mul));
+        ob = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (gr < rows) {
+        if (gc < K) *reinterpret_cast<uint4*>(col_codes + gc * rows + gr) = oa;
+        if (gc + 1 < K) *reinterpret_cast<uint4*>(col_codes + (gc + 1) * rows + gr) = ob;
+    }
+    // blocks of a column: row groups 0, 2, 4, 6 hold blocks 0..3 of the tile (lanes 8 apart)
+    mx_store_sf4(col_sf, SWZ, gc, row0 >> 5, nsf_col, sa, 8, g == 0, gc < K && row0 < rows);
+    mx_store_sf4(col_sf, SWZ, gc + 1, row0 >> 5, nsf_col, sb, 8, g == 0, gc + 1 < K && row0 < rows);
 }
 
 // Zero the padding of a swizzled SF buffer (rows and columns beyond the

@@ -133,7 +133,9 @@ bsq_status quantize_nvfp4_per_expert(const void* w, int64_t experts, int64_t row
  * condiviso ...": blocks follow the reduction dimension).  Shared exponent:
  * X = clamp(floor(log2(amax)) - 8, -127, 127), SF = X + 127, codes =
  * E4M3(x * 2^-X), round to nearest even, saturating at 448.
- *   x          bf16 [rows][ldx]; rows % 32 == 0, K % 32 == 0, ldx % 8 == 0
+ *   x          bf16 [rows][ldx]; rows % 32 == 0, K % 32 == 0, ldx % 8 == 0;
+ *              x and the code buffers 16-byte aligned, the SF buffers 4-byte
+ *              aligned (else BSQ_ERR_ALIGN)
  *   row_codes  out, E4M3 [rows][K] (NULL: skip the row copy with row_sf)
  *   row_sf     out, E8M0 [rows][K/32] linear or swizzled
  *   col_codes  out, E4M3 [K][rows] (the column copy, stored transposed;
