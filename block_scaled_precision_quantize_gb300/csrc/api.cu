@@ -281,7 +281,7 @@ bsq_status bsq_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, 
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0 || topk > 32) return BSQ_ERR_SHAPE;
     std::memset(L, 0, sizeof(*L));
     const int64_t cap = moe_capacity(T, E, topk);
-    const int64_t nchunks = (T * topk + 4095) / 4096;
+    const int64_t nchunks = (T * topk + 511) / 512;  // routing chunk of 512 pairs
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -301,7 +301,7 @@ bsq_status bsq_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, 
     L->hq_sf = take((size_t)cap * ((I / 16 + 3) / 4 * 4));
     L->hq_scale = take((size_t)cap * 4);
     L->out = take((size_t)cap * H * 2);
-    L->scan = take((size_t)std::max<int64_t>(nchunks, 1) * E * 4);
+    L->scan = take(((size_t)std::max<int64_t>(nchunks, 1) * E + 1) * 4);  // histograms + ticket
     L->total = o;
     return BSQ_OK;
 }

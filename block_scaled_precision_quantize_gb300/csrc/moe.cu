@@ -12,14 +12,17 @@
 
 namespace bsq {
 
-constexpr int RT_CHUNK = 4096;  // routed pairs per histogram chunk
+constexpr int RT_CHUNK = 512;  // routed pairs per histogram chunk
 
-// Phase A: per-chunk expert histograms -> hist[chunk][E].
+// Phase A: per-chunk expert histograms -> hist[chunk][E].  Also clears the
+// ticket counter of phase B (stream order puts this before phase B).
 __global__ void __launch_bounds__(256) k_route_hist(const int32_t* __restrict__ ids, int64_t n, int32_t E,
-                                                    int32_t* __restrict__ hist, int32_t* dev_status)
+                                                    int32_t* __restrict__ hist, int32_t* __restrict__ ticket,
+                                                    int32_t* dev_status)
 {
     extern __shared__ int32_t sh[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
     __syncthreads();
     const int64_t i0 = (int64_t)blockIdx.x * RT_CHUNK, i1 = min(n, i0 + RT_CHUNK);
     for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
@@ -31,40 +34,71 @@ __global__ void __launch_bounds__(256) k_route_hist(const int32_t* __restrict__ 
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = sh[e];
 }
 
-// Phase B (one CTA of 1024 threads): per expert, exclusive prefix of the chunk
-// histograms (in place) and the total; then the padded segment offsets.
-__global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ hist, int32_t nchunks, int32_t E,
-                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets)
+// Exclusive prefix of v over the 256 threads of a CTA; *total gets the sum.
+__device__ __forceinline__ int32_t block_exclusive_scan256(int32_t v, int32_t* warp_sums, int32_t* total)
 {
-    __shared__ int32_t part[1024];
-    __shared__ int32_t carry;
-    if (threadIdx.x == 0) carry = 0;
-    for (int e0 = 0; e0 < E; e0 += 1024) {
-        const int e = e0 + threadIdx.x;
-        int32_t total = 0;
-        if (e < E) {
-            for (int c = 0; c < nchunks; ++c) {
-                const int32_t v = hist[(int64_t)c * E + e];
-                hist[(int64_t)c * E + e] = total;
-                total += v;
-            }
-            counts[e] = total;
-        }
-        const int32_t padded = (e < E) ? ((total + 127) & ~127) : 0;
-        part[threadIdx.x] = padded;
-        __syncthreads();
-        for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
-            const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-            __syncthreads();
-            part[threadIdx.x] += v;
-            __syncthreads();
-        }
-        if (e < E) offsets[e] = carry + part[threadIdx.x] - padded;
-        __syncthreads();
-        if (threadIdx.x == 1023) carry += part[1023];
-        __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += u;
     }
-    if (threadIdx.x == 0) offsets[E] = carry;
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int32_t ws = warp_sums[w];
+        before += (w < warp) ? ws : 0;
+        all += ws;
+    }
+    __syncthreads();
+    *total = all;
+    return before + incl - v;
+}
+
+// Phase B: CTA e turns column e of hist into its exclusive prefix over the
+// chunks (in place) and writes counts[e]; the last CTA to finish (ticket)
+// then lays out the segments: offsets[e] = sum over e' < e of counts[e']
+// rounded up to 128, offsets[E] = the total.
+__global__ void __launch_bounds__(256) k_route_scan(int32_t* __restrict__ hist, int32_t nchunks, int32_t E,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ ticket)
+{
+    __shared__ int32_t warp_sums[8];
+    __shared__ bool last;
+    const int e = blockIdx.x;
+    int32_t carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 256) {
+        const int c = c0 + threadIdx.x;
+        const int32_t v = c < nchunks ? hist[(int64_t)c * E + e] : 0;
+        int32_t total;
+        const int32_t ex = block_exclusive_scan256(v, warp_sums, &total);
+        if (c < nchunks) hist[(int64_t)c * E + e] = carry + ex;
+        carry += total;
+    }
+    if (threadIdx.x == 0) {
+        counts[e] = carry;
+        __threadfence();
+        last = atomicAdd(ticket, 1) == E - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    int32_t base = 0;
+    for (int e0 = 0; e0 < E; e0 += 256) {
+        const int ee = e0 + threadIdx.x;
+        const int32_t padded = ee < E ? ((__ldcg(counts + ee) + 127) & ~127) : 0;
+        int32_t total;
+        const int32_t ex = block_exclusive_scan256(padded, warp_sums, &total);
+        if (ee < E) offsets[ee] = base + ex;
+        base += total;
+    }
+    if (threadIdx.x == 0) {
+        offsets[E] = base;
+        *ticket = 0;
+    }
 }
 
 // Phase C: one warp per chunk walks its pairs in order, 32 at a time; lanes
@@ -139,20 +173,15 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
         rmax = __reduce_max_sync(0xFFFFFFFFu, rmax);
         const float tt = __fdiv_rn(bf16mag_to_f32(rmax), kNvfp4ScaleDivisor);
         const float six_t = __fmul_rn(6.0f, tt), four_t = __fmul_rn(4.0f, tt);
-        int32_t slots[32];
-        int nslots = 0;
-        for (int j = 0; j < topk; ++j) {
-            const int32_t s = __ldg(slot_of + t * topk + j);
-            if (s >= 0) slots[nslots++] = s;
-        }
-        if (lane < nslots) scale[slots[lane]] = tt;
+        // lane j < topk holds the slot of pair (t, j) (-1: not routed)
+        const int32_t my_slot = lane < topk ? __ldg(slot_of + t * topk + lane) : -1;
+        if (my_slot >= 0) scale[my_slot] = tt;
 #pragma unroll
         for (int i = 0; i < BPL; ++i) {
             const int b = lane + 32 * i;
-            if (b >= nblk) continue;
             uint2 c = make_uint2(0u, 0u);
             uint32_t s = 0;
-            if (tt != 0.0f) {
+            if (b < nblk && tt != 0.0f) {
                 float xs[16];
                 const uint32_t w[8] = {va[i].x, va[i].y, va[i].z, va[i].w, vb[i].x, vb[i].y, vb[i].z, vb[i].w};
 #pragma unroll
@@ -173,10 +202,17 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                     }
                 }
             }
-            for (int j = 0; j < nslots; ++j) {
-                const int64_t r = slots[j];
-                reinterpret_cast<uint2*>(codes + r * (H >> 1))[b] = c;
-                sf[sf_swizzled(r, b, ncol_tiles)] = (uint8_t)s;
+            // the 4 scale bytes of blocks b .. b+3 (lanes b .. b+3) as one word:
+            // consecutive in the swizzled layout, b % 4 == 0 at the gathering lane
+            const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, s, 1);
+            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, s, 2);
+            const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, s, 3);
+            const uint32_t sw = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            for (int j = 0; j < topk; ++j) {
+                const int32_t r = __shfl_sync(0xFFFFFFFFu, my_slot, j);
+                if (r < 0 || b >= nblk) continue;
+                reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1))[b] = c;
+                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_swizzled(r, b, ncol_tiles)) = sw;
             }
         }
     }
@@ -239,9 +275,14 @@ void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_
 {
     const int64_t n = T * topk;
     const int nchunks = (int)((n + RT_CHUNK - 1) / RT_CHUNK);
+    int32_t* ticket = hist + (int64_t)std::max(nchunks, 1) * E;  // one word after the histograms
     cudaMemsetAsync(row_src, 0xFF, (size_t)capacity * sizeof(int32_t), st);
-    if (nchunks > 0) k_route_hist<<<nchunks, 256, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, dev_status);
-    k_route_scan<<<1, 1024, 0, st>>>(hist, nchunks, E, counts, offsets);
+    if (nchunks > 0) {
+        k_route_hist<<<nchunks, 256, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, ticket, dev_status);
+    } else {
+        cudaMemsetAsync(ticket, 0, sizeof(int32_t), st);
+    }
+    k_route_scan<<<E, 256, 0, st>>>(hist, nchunks, E, counts, offsets, ticket);
     if (nchunks > 0)
         k_route_assign<<<nchunks, 32, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, offsets, slot_of, row_src);
 }

@@ -269,7 +269,8 @@ typedef struct {
     size_t hq_sf;        /* u8 swizzled, cap x I/16 */
     size_t hq_scale;     /* fp32 [cap] */
     size_t out;          /* bf16 [cap][H] per-slot expert outputs */
-    size_t scan;         /* int32 scratch for the routing scan */
+    size_t scan;         /* int32 scratch for the routing scan: per-512-pair
+                            chunk expert histograms and a counter */
     size_t total;        /* bytes */
     int64_t capacity;    /* cap: T*topk + E*127 rounded up to 128 */
 } bsq_moe_layout;

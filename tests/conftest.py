@@ -31,7 +31,8 @@ def O():
 @pytest.fixture(scope="session")
 def gpu():
     """The CUDA library on a GPU; the test is skipped only when there is no
-    GPU at all. On a GPU machine a missing library is an error, not a skip."""
+    GPU at all. On a machine with a GPU a missing library is an error, not a
+    skip."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
