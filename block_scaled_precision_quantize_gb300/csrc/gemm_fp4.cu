@@ -55,9 +55,9 @@
 
 namespace bsq {
 
-constexpr int GM_SF_WARPS = 4;
+constexpr int GM_SF_WARPS = 3;
 constexpr int GM_EPI_WARPS = 16;
-constexpr int GM_THREADS = 32 * (2 + GM_SF_WARPS + GM_EPI_WARPS);  // 704
+constexpr int GM_THREADS = 32 * (2 + GM_SF_WARPS + GM_EPI_WARPS);  // 672
 constexpr int GM_STAGES = 3;
 constexpr int GM_SFA_OFF = 0;
 constexpr int GM_SFB_OFF = 2048;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[4 * GM_STAGES + 3];
+    __shared__ __align__(8) uint64_t bars[4 * GM_STAGES + 3 + GM_SF_WARPS];
     __shared__ int32_t s_off[GM_MAX_SMEM_EXPERTS + 1];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort, s_bad;
@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     const uint32_t acc_full = bar0 + 8u * (4 * GM_STAGES);
     const uint32_t acc_empty = bar0 + 8u * (4 * GM_STAGES + 1);
     const uint32_t drain_bar = bar0 + 8u * (4 * GM_STAGES + 2);
+    auto sf_drain = [&](int w) { return bar0 + 8u * (uint32_t)(4 * GM_STAGES + 3 + w); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < GM_STAGES; ++s) {
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, GM_EPI_WARPS);
         mbar_init(drain_bar, 1);
+        for (int w = 0; w < GM_SF_WARPS; ++w) mbar_init(sf_drain(w), 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -493,52 +495,46 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         __syncwarp();
     } else if (warp < 2 + GM_SF_WARPS) {
         // ------------------------------------------------------ scale factors -> tensor memory
-        // Lane l of the quadrant-q warp writes, for tensor-memory lane 32q + l,
-        // row l of every 512-byte SF chunk of the stage (16 bytes = 4 columns).
-        // The SF copies have their own barrier and are issued before the
-        // stage's codes, so this runs while the codes are still in flight.
-        const int q = warp & 3;
-        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + GM_SF_RING;
-        uint32_t it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            for (int kt = 0; kt < kt_count; ++kt, ++it) {
-                const int s = (int)(it % GM_STAGES);
-                const uint32_t ph = (it / GM_STAGES) & 1u;
-                // implies the slot's previous scale factors were consumed: the producer
-                // refills a stage only after the MMAs that read it completed
-                const bool ok = mbar_wait(sf_full(s), ph, abort_flag);
-                if (!__all_sync(0xFFFFFFFFu, ok)) {
-                    if (lane == 0) {
+        // One lane of each of these three warps moves a third of a stage's
+        // scale factors into the tensor-memory ring with tcgen05.cp
+        // 32x128b.warpx4 (each 512-byte chunk lands in all four lane
+        // quadrants, the layout the block-scaled MMA reads): warp 2 A's four
+        // chunks (columns 4j), warps 3 and 4 B's first and second 128 rows
+        // (columns 16 + 8j and 20 + 8j), then commits them to the stage's SF
+        // barrier.  The copies start as soon as the SF land, while the codes
+        // are still in flight, and they neither pass through registers nor
+        // cost shared-memory reads beyond the 6 KB themselves.
+        const int which = warp - 2;  // 0: A, 1: B rows 0-127, 2: B rows 128-255
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+                for (int kt = 0; kt < kt_count; ++kt, ++it) {
+                    const int s = (int)(it % GM_STAGES);
+                    const uint32_t ph = (it / GM_STAGES) & 1u;
+                    // implies the slot's previous scale factors were consumed: the producer
+                    // refills a stage only after the MMAs that read it completed
+                    if (!mbar_wait(sf_full(s), ph, abort_flag)) {
                         *abort_flag = 1;
                         report(p.dev_status, BSQ_DEV_TIMEOUT);
+                        break;
                     }
-                    break;
-                }
-                tc_fence_after();
-                const uint8_t* sp = smem + (size_t)s * GM_STAGE_BYTES + 16 * lane;
-                uint32_t ra[16], rb[32];
+                    tc_fence_after();
+                    const uint32_t src = sbase + (uint32_t)s * GM_STAGE_BYTES +
+                                         (which == 0 ? GM_SFA_OFF : GM_SFB_OFF + 2048 * (which - 1));
+                    const uint32_t dst = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS +
+                                         (which == 0 ? 0u : 16u + 4u * (uint32_t)(which - 1));
+                    const uint32_t step = which == 0 ? 4u : 8u;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // A: chunk row l holds rows l, l+32, l+64, l+96 in its four
-                    // columns, and the quadrant-q lanes (rows 32q + l) read only
-                    // column q, so one 4-byte word per chunk fills this quadrant
-                    const uint32_t va = *reinterpret_cast<const uint32_t*>(sp + GM_SFA_OFF + 512 * j + 4 * q);
-                    const uint4 v0 = *reinterpret_cast<const uint4*>(sp + GM_SFB_OFF + 512 * j);
-                    const uint4 v1 = *reinterpret_cast<const uint4*>(sp + GM_SFB_OFF + 2048 + 512 * j);
-                    ra[4 * j] = va; ra[4 * j + 1] = va; ra[4 * j + 2] = va; ra[4 * j + 3] = va;
-                    rb[8 * j] = v0.x; rb[8 * j + 1] = v0.y; rb[8 * j + 2] = v0.z; rb[8 * j + 3] = v0.w;
-                    rb[8 * j + 4] = v1.x; rb[8 * j + 5] = v1.y; rb[8 * j + 6] = v1.z; rb[8 * j + 7] = v1.w;
+                    for (int j = 0; j < 4; ++j) tc_cp_sf(dst + step * j, smem_desc(src + 512 * j, 16, 128, 0));
+                    tc_commit(sf_bar(s));
                 }
-                const uint32_t col = tq + (uint32_t)s * GM_SF_STAGE_COLS;
-                tc_st16(col, ra);
-                tc_st16(col + 16, rb);
-                tc_st16(col + 32, rb + 16);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sf_bar(s));
             }
+            // every copy issued here lands before tensor memory is freed
+            tc_commit(sf_drain(which));
+            for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
+                if (mbar_try_wait(sf_drain(which), 0u)) break;
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;                                  // tensor-memory lane quadrant
