@@ -243,18 +243,35 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ ou
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+        // lane j < topk holds pair (t, j)'s slot and weight; broadcast below so
+        // that a lane issues the loads of all k expert rows back to back
+        const int32_t my_slot = lane < topk ? __ldg(slot_of + t * topk + lane) : -1;
+        const float my_w = lane < topk ? __ldg(w + t * topk + lane) : 0.0f;
         for (int64_t c = 8 * lane; c < H; c += 256) {
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < topk; ++j) {
-                const int32_t s = __ldg(slot_of + t * topk + j);
-                if (s < 0) continue;
-                const float wj = __ldg(w + t * topk + j);
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(out + (int64_t)s * H + c));
-                const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+            for (int j0 = 0; j0 < topk; j0 += 8) {
+                uint4 v[8];
+                float wj[8];
+                bool has[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wj, bf16_lo(q[i])));
-                    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wj, bf16_hi(q[i])));
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = j0 + jj;
+                    const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, j & 31);
+                    wj[jj] = __shfl_sync(0xFFFFFFFFu, my_w, j & 31);
+                    has[jj] = j < topk && s >= 0;
+                    v[jj] = has[jj] ? __ldg(reinterpret_cast<const uint4*>(out + (int64_t)s * H + c))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                }
+                // fixed order j = 0, 1, ...; pairs without a slot are skipped
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    if (!has[jj]) continue;
+                    const uint32_t q[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wj[jj], bf16_lo(q[i])));
+                        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wj[jj], bf16_hi(q[i])));
+                    }
                 }
             }
             uint4 o;

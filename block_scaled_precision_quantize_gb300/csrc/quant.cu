@@ -82,26 +82,32 @@ BSQ_DEVICE void store_sf(uint8_t* sf, bool swz, int64_t row, int64_t col, int64_
 }
 
 // ---------------------------------------------------------------------------
-// Per-row NVFP4, one warp per row.  Lane l owns blocks l, l+32, ... (BPL of
-// them); the warp reads 1 KB contiguous per step.  TMODE 0: per-row scale from
-// the row maximum; TMODE 1: per-group scale from group_amax[row / rpg].
+// Per-row NVFP4 with LPR lanes per row (32: one warp per row; 16: each
+// half-warp takes a row, for row lengths whose block count is an odd multiple
+// of 16, so no lane idles).  Lane l of a row owns blocks l, l+LPR, ... (BPL of
+// them) and reads them with 16-byte streaming loads.  TMODE 0: per-row scale
+// from the row maximum; TMODE 1: per-group scale from group_amax[row / rpg].
 // With SWZ the padding rows up to a multiple of 128 and the padding SF
 // columns are written as 0.
-template <int BPL, bool FOUR_SIX, bool SWZ, int TMODE>
+template <int BPL, bool FOUR_SIX, bool SWZ, int TMODE, int LPR = 32>
 __global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                     int64_t ldx, uint8_t* __restrict__ codes,
                                                     uint8_t* __restrict__ sf, float* __restrict__ row_scale,
                                                     const float* __restrict__ group_amax, int64_t rpg)
 {
-    const int lane = threadIdx.x & 31;
+    constexpr int RPW = 32 / LPR;  // rows per warp step
+    const int lane = threadIdx.x & 31, lr = lane % LPR;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int nblk = (int)(K >> 4);
     const int ncol_pad = SWZ ? ((nblk + 3) & ~3) : nblk;
     const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows_iter; r += nwarps) {
-        if (r >= rows) {  // swizzle padding rows
-            for (int b = lane; b < ncol_pad; b += 32) store_sf(sf, SWZ, r, b, nblk, 0u);
-            continue;
+    // warp-uniform loop over groups of RPW rows (the shuffles below need all lanes)
+    for (int64_t r0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * RPW; r0 < rows_iter;
+         r0 += nwarps * RPW) {
+        const int64_t r = r0 + lane / LPR;
+        const bool in_iter = r < rows_iter, real = r < rows;
+        if (in_iter && !real) {  // swizzle padding rows
+            for (int b = lr; b < ncol_pad; b += LPR) store_sf(sf, SWZ, r, b, nblk, 0u);
         }
         const uint16_t* xr = x + r * ldx;
         uint4 va[BPL], vb[BPL];
@@ -109,8 +115,8 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__
         uint32_t rmax = 0;
 #pragma unroll
         for (int i = 0; i < BPL; ++i) {
-            const int b = lane + 32 * i;
-            if (b < nblk) {
+            const int b = lr + LPR * i;
+            if (real && b < nblk) {
                 va[i] = ldg_stream(xr + 16 * b);
                 vb[i] = ldg_stream(xr + 16 * b + 8);
             } else {
@@ -124,17 +130,19 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__
         }
         float t;
         if (TMODE == 0) {
-            rmax = __reduce_max_sync(0xFFFFFFFFu, rmax);
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) rmax = max(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, off));
             t = __fdiv_rn(bf16mag_to_f32(rmax), kNvfp4ScaleDivisor);
-            if (lane == 0) row_scale[r] = t;
+            if (lr == 0 && real) row_scale[r] = t;
         } else {
-            t = __fdiv_rn(group_amax[r / rpg], kNvfp4ScaleDivisor);
+            t = real ? __fdiv_rn(group_amax[r / rpg], kNvfp4ScaleDivisor) : 0.0f;
         }
+        if (!real) continue;
         const float six_t = __fmul_rn(6.0f, t), four_t = __fmul_rn(4.0f, t);
         uint2* crow = reinterpret_cast<uint2*>(codes + r * (K >> 1));
 #pragma unroll
         for (int i = 0; i < BPL; ++i) {
-            const int b = lane + 32 * i;
+            const int b = lr + LPR * i;
             if (b < nblk) {
                 uint2 c;
                 uint32_t s;
@@ -706,7 +714,10 @@ static void launch_rows_t(const uint16_t* x, int64_t rows, int64_t K, int64_t ld
     const int nblk = (int)(K >> 4);
     const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
     const int grid = grid_for(rows_iter, sms);
-    if (nblk <= 32)
+    if (nblk == 48)  // e.g. K = 768: a half-warp per row, 3 blocks per lane
+        k_nvfp4_rows<3, F46, SWZ, TM, 16><<<grid_for((rows_iter + 1) / 2, sms), 256, 0, st>>>(x, rows, K, ldx, codes, sf,
+                                                                                               rs, gam, rpg);
+    else if (nblk <= 32)
         k_nvfp4_rows<1, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 64)
         k_nvfp4_rows<2, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
