@@ -183,3 +183,110 @@ def test_moe_qwen3_shaped_sampled(gpu, O):
                  g.choice(int(offsets[-1]), 192, replace=False)]
         return np.unique(np.concatenate(picks))
     _staged(gpu, O, T=16384, H=2048, I=768, E=128, k=8, four_six=False, seed=3, sample_rows=sample)
+
+
+def test_moe_deepseek_shaped_sampled(gpu, O):
+    """The DeepSeek-V3-shaped layer at full size (T=32768, H=7168, E=256,
+    top-8 with a Zipf-skewed expert bias s=1.1, I=2048, 4/6 on the
+    activations), weights drawn on the device.  Routing is checked in full;
+    the later stages on sampled rows of four experts (the most and the least
+    loaded and two random ones), whose weights alone go through the oracle.
+    Per-token quantization is row-independent, so the oracle quantizes only
+    the tokens those rows come from."""
+    T, H, I, E, k, seed = 32768, 7168, 2048, 256, 8, 5
+    x = synth.normal((T, H), seed=seed)
+    ids, wts = synth.topk_routing(T, E, k, seed=seed, zipf_s=1.1)
+    wgu_d = synth.device_normal_bf16((E, 2 * I, H), seed=51, std=0.02)
+    wd_d = synth.device_normal_bf16((E, H, I), seed=52, std=0.02)
+    wgu = gpu.quantize_nvfp4_per_expert(wgu_d)
+    wd = gpu.quantize_nvfp4_per_expert(wd_d)
+    L = gpu.moe_workspace_layout(T, H, I, E, k)
+    ws = torch.zeros(L.total, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, four_six=True, workspace=ws,
+                               dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    cap = L.capacity
+
+    # 1. routing (all pairs)
+    offsets, slot_of, row_src = O.route(ids, E)
+    R = int(offsets[-1])
+    assert bits_equal(_ws(ws, L, "offsets", np.int32, (E + 1,)), offsets)
+    assert bits_equal(_ws(ws, L, "slot_of", np.int32, (T * k,)), slot_of)
+    assert bits_equal(_ws(ws, L, "row_src", np.int32, (cap,))[:R], row_src)
+
+    # sampled rows: 32 from each of four experts (a segment holds its routed
+    # rows first, then the padding up to a multiple of 128)
+    counts = np.bincount(ids.ravel(), minlength=E)
+    g = np.random.default_rng(1)
+    big, small = int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    others = [e for e in g.permutation(E) if counts[e] >= 32 and e not in (big, small)][:2]
+    experts = [big, small] + [int(e) for e in others]
+    rows = np.concatenate([offsets[e] + g.choice(int(counts[e]), min(32, int(counts[e])), replace=False)
+                           for e in experts])
+    src_tok = row_src[rows] // k
+    assert np.all(row_src[rows] >= 0)
+
+    # the sampled experts' weights, quantized by the oracle and checked bit-exact
+    # against the GPU per-expert quantizer
+    def expert_q(w_d, q, e):
+        wb = to_np(w_d[e:e + 1].contiguous().view(torch.int16)).view(np.uint16)
+        c, s, t = O.nvfp4_quantize_group(wb)
+        N, Kc = w_d.shape[1], w_d.shape[2]
+        assert bits_equal(to_np(q[0][e]), c[0]) and bits_equal(to_np(q[2][e:e + 1]), t)
+        sf_all = to_np(q[1])
+        nct = (Kc // 16 + 3) // 4
+        tile_bytes = nct * 512
+        r0 = e * N  # expert e's rows start on a 128-row tile boundary (N % 128 == 0)
+        sf_e = _unswz(O, sf_all[(r0 // 128) * tile_bytes:((r0 + N) // 128) * tile_bytes], N, Kc // 16)
+        assert bits_equal(sf_e, s[0])
+        return c[0], s[0], t[0]
+
+    # 2. quantize-scatter of the sampled rows' tokens, with 4/6
+    xc, xs, xt = O.nvfp4_quantize_rows(x[src_tok], four_six=True)
+    q_codes = _ws(ws, L, "xq_codes", np.uint8, (cap, H // 2))[rows]
+    q_scale = _ws(ws, L, "xq_scale", np.float32, (cap,))[rows]
+    q_sf = _unswz(O, _ws(ws, L, "xq_sf", np.uint8, (cap * (H // 16),)), cap, H // 16)[rows]
+    assert bits_equal(q_codes, xc), first_mismatch(q_codes, xc)
+    assert bits_equal(q_sf, xs) and bits_equal(q_scale, xt)
+
+    h_gpu = _ws(ws, L, "h", np.uint16, (cap, I))
+    hq_codes = _ws(ws, L, "hq_codes", np.uint8, (cap, I // 2))
+    hq_scale = _ws(ws, L, "hq_scale", np.float32, (cap,))
+    hq_sf = _unswz(O, _ws(ws, L, "hq_sf", np.uint8, (cap * (I // 16),)), cap, I // 16)
+    out_gpu = _ws(ws, L, "out", np.uint16, (cap, H))
+    base = 0
+    for e in experts:
+        n = min(32, int(counts[e]))
+        sel = slice(base, base + n)
+        rr = rows[sel]
+        base += n
+        GUe = expert_q(wgu_d, wgu, e)
+        # 3. GEMM1 + SwiGLU on the oracle's own quantized x
+        o, a = O.gemm_nvfp4(xc[sel], xs[sel], xt[sel], *GUe)
+        h_ref = O.swiglu(o)
+        gg, uu = o[:, :I], o[:, I:]
+        sg = gg / (1 + np.exp(-gg))
+        bound = 1.1 * np.abs(uu) * 1e-4 * a[:, :I] + np.abs(sg) * 1e-4 * a[:, I:] + 2.0 ** -8 * np.abs(h_ref) + 1e-30
+        hg = synth.bf16_bits_to_f32(h_gpu[rr]).astype(np.float64)
+        assert np.all(np.abs(hg - h_ref) <= bound), (e, np.max(np.abs(hg - h_ref) / bound))
+        # 4. quantization of the GPU's own h, with 4/6 (bit-exact)
+        hc, hs, ht = O.nvfp4_quantize_rows(h_gpu[rr], four_six=True)
+        assert bits_equal(hq_codes[rr], hc) and bits_equal(hq_sf[rr], hs) and bits_equal(hq_scale[rr], ht), e
+        # 5. GEMM2 from the GPU's own quantized h
+        DNe = expert_q(wd_d, wd, e)
+        o2, a2 = O.gemm_nvfp4(hq_codes[rr], hq_sf[rr], hq_scale[rr], *DNe)
+        got = synth.bf16_bits_to_f32(out_gpu[rr]).astype(np.float64)
+        assert np.all(np.abs(got - o2) <= _bf16_bound(o2, a2)), e
+
+    # 6. combine of the GPU's own expert outputs, for the sampled rows' tokens
+    toks = np.unique(src_tok)
+    s_t = slot_of.reshape(T, k)[toks]
+    w_t = wts[toks]
+    y_ref = O.combine(out_gpu, s_t.reshape(-1), w_t)
+    yg = synth.bf16_bits_to_f32(to_np(y)[toks]).astype(np.float64)
+    yr = synth.bf16_bits_to_f32(y_ref).astype(np.float64)
+    of = synth.bf16_bits_to_f32(out_gpu[s_t]).astype(np.float64)  # [tokens, k, H]: the sampled tokens only
+    terms = np.abs(of * w_t[:, :, None]).sum(axis=1)
+    assert np.all(np.abs(yg - yr) <= 2.0 ** -7 * np.abs(yr) + 1e-6 * terms + 1e-30)
