@@ -251,15 +251,33 @@ BSQ_DEVICE BlockScale nvfp4_block_scale(float amax_b, float mult_t, float t)
     return b;
 }
 
+// Eight E2M1 codes (nibble i = element i) decoded to binary32 with the
+// hardware conversion to f16 pairs (exact: E2M1 values are f16 values).
+BSQ_DEVICE void e2m1x8_to_f32(uint32_t w, float* v)
+{
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
 // Squared error of a candidate block (codes packed 8 per word), summed by the
 // fixed tree p_j = s_j + s_{j+8}, q_j = p_j + p_{j+4}, r_j = q_j + q_{j+2}.
 BSQ_DEVICE float block_sse(const float x[16], uint32_t c_lo, uint32_t c_hi, float d)
 {
-    float sq[16];
+    float v[16], sq[16];
+    e2m1x8_to_f32(c_lo, v);
+    e2m1x8_to_f32(c_hi, v + 8);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const uint32_t nib = ((i < 8 ? c_lo : c_hi) >> (4 * (i & 7))) & 0xFu;
-        const float e = __fsub_rn(x[i], __fmul_rn(e2m1_to_f32(nib), d));
+        const float e = __fsub_rn(x[i], __fmul_rn(v[i], d));
         sq[i] = __fmul_rn(e, e);
     }
     float p[8], q[4];
@@ -269,8 +287,6 @@ BSQ_DEVICE float block_sse(const float x[16], uint32_t c_lo, uint32_t c_hi, floa
     for (int j = 0; j < 4; ++j) q[j] = __fadd_rn(p[j], p[j + 4]);
     return __fadd_rn(__fadd_rn(q[0], q[2]), __fadd_rn(q[1], q[3]));
 }
-
-// Quantize 16 values with a block scale; returns the two code words.
 BSQ_DEVICE uint2 encode16(const float x[16], float enc)
 {
     float q[16];
