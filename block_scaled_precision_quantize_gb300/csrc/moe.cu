@@ -134,25 +134,35 @@ __global__ void __launch_bounds__(32) k_route_assign(const int32_t* __restrict__
 
 // Per-token NVFP4 quantization of x, written to every routed slot of the
 // token (one warp per token, lane l owns 16-blocks l, l+32, ...).
-template <int BPL, bool FOUR_SIX>
+// WPR warps share a token (wide rows: a row of 448 blocks at 4 blocks per
+// lane instead of 16 keeps the registers, and so the occupancy, reasonable);
+// a CTA of 8 warps takes 8 / WPR tokens per step and the row maximum is folded
+// across the token's warps in shared memory.  Lane l of part p of a token owns
+// blocks 32 p + l + 32 WPR i.
+template <int BPL, bool FOUR_SIX, int WPR = 1>
 __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, int64_t T, int64_t H,
                                                        int32_t topk, const int32_t* __restrict__ slot_of,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                        float* __restrict__ scale)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    constexpr int TPC = 8 / WPR;  // tokens per CTA step
+    __shared__ uint32_t part_max[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int part = warp % WPR, li = 32 * part + lane;
     const int nblk = (int)(H >> 4);
     const int64_t ncol_tiles = (nblk + 3) >> 2;
-    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    // CTA-uniform loop (the shared-memory fold below synchronizes the CTA)
+    for (int64_t t0 = (int64_t)blockIdx.x * TPC; t0 < T; t0 += (int64_t)gridDim.x * TPC) {
+        const int64_t t = t0 + warp / WPR;
+        const bool real = t < T;
         const uint16_t* xr = x + t * H;
         uint4 va[BPL], vb[BPL];
         uint32_t bmax[BPL];
         uint32_t rmax = 0;
 #pragma unroll
         for (int i = 0; i < BPL; ++i) {
-            const int b = lane + 32 * i;
-            if (b < nblk) {
+            const int b = li + 32 * WPR * i;
+            if (real && b < nblk) {
                 asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(va[i].x), "=r"(va[i].y), "=r"(va[i].z), "=r"(va[i].w) : "l"(xr + 16 * b));
                 asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -171,14 +181,23 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
             rmax = max(rmax, bmax[i]);
         }
         rmax = __reduce_max_sync(0xFFFFFFFFu, rmax);
+        if (WPR > 1) {
+            if (lane == 0) part_max[warp] = rmax;
+            __syncthreads();
+            const int w0 = warp - part;
+#pragma unroll
+            for (int p = 0; p < WPR; ++p) rmax = max(rmax, part_max[w0 + p]);
+            __syncthreads();
+        }
+        if (!real) continue;
         const float tt = __fdiv_rn(bf16mag_to_f32(rmax), kNvfp4ScaleDivisor);
         const float six_t = __fmul_rn(6.0f, tt), four_t = __fmul_rn(4.0f, tt);
         // lane j < topk holds the slot of pair (t, j) (-1: not routed)
         const int32_t my_slot = lane < topk ? __ldg(slot_of + t * topk + lane) : -1;
-        if (my_slot >= 0) scale[my_slot] = tt;
+        if (my_slot >= 0 && part == 0) scale[my_slot] = tt;
 #pragma unroll
         for (int i = 0; i < BPL; ++i) {
-            const int b = lane + 32 * i;
+            const int b = li + 32 * WPR * i;
             uint2 c = make_uint2(0u, 0u);
             uint32_t s = 0;
             if (b < nblk && tt != 0.0f) {
@@ -317,8 +336,11 @@ void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk,
     if (nblk <= 32) BSQ_QS(1);
     else if (nblk <= 64) BSQ_QS(2);
     else if (nblk <= 128) BSQ_QS(4);
-    else if (nblk <= 256) BSQ_QS(8);
-    else BSQ_QS(16);
+    else {  // wide rows: 4 warps per token, up to 4 blocks per lane (H <= 8192)
+        const int grid4 = (int)std::max<int64_t>(1, std::min<int64_t>((T + 1) / 2, (int64_t)sms * 16));
+        if (four_six) k_quant_scatter<4, true, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);
+        else k_quant_scatter<4, false, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);
+    }
 #undef BSQ_QS
 }
 
