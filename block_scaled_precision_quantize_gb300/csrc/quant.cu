@@ -156,6 +156,83 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__
     }
 }
 
+// Wide rows (128 < blocks <= 512): four warps per row, up to four blocks per
+// lane (one warp per row would need 8-16 blocks per lane, i.e. more registers
+// and so fewer warps in flight).  A CTA of 8 warps takes 2 rows per step; the
+// row maximum is folded across the row's warps in shared memory.  Lane l of
+// part p owns blocks 32 p + l + 128 i.
+template <bool FOUR_SIX, bool SWZ, int TMODE>
+__global__ void __launch_bounds__(256) k_nvfp4_rows_wide(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                         int64_t ldx, uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ sf, float* __restrict__ row_scale,
+                                                         const float* __restrict__ group_amax, int64_t rpg)
+{
+    constexpr int WPR = 4, BPL = 4;
+    __shared__ uint32_t part_max[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int part = warp % WPR, li = 32 * part + lane;
+    const int nblk = (int)(K >> 4);
+    const int ncol_pad = SWZ ? ((nblk + 3) & ~3) : nblk;
+    const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
+    // CTA-uniform loop over pairs of rows (the shared-memory fold synchronizes the CTA)
+    for (int64_t r0 = (int64_t)blockIdx.x * 2; r0 < rows_iter; r0 += (int64_t)gridDim.x * 2) {
+        const int64_t r = r0 + warp / WPR;
+        const bool in_iter = r < rows_iter, real = r < rows;
+        if (in_iter && !real) {  // swizzle padding rows
+            for (int b = li; b < ncol_pad; b += 32 * WPR) store_sf(sf, SWZ, r, b, nblk, 0u);
+        }
+        const uint16_t* xr = x + r * ldx;
+        uint4 va[BPL], vb[BPL];
+        uint32_t bmax[BPL];
+        uint32_t rmax = 0;
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            const int b = li + 32 * WPR * i;
+            if (real && b < nblk) {
+                va[i] = ldg_stream(xr + 16 * b);
+                vb[i] = ldg_stream(xr + 16 * b + 8);
+            } else {
+                va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            bmax[i] = absmax16(va[i], vb[i]);
+            rmax = max(rmax, bmax[i]);
+        }
+        float t = 0.0f;
+        if (TMODE == 0) {
+            rmax = __reduce_max_sync(0xFFFFFFFFu, rmax);
+            if (lane == 0) part_max[warp] = rmax;
+            __syncthreads();
+            const int w0 = warp - part;
+#pragma unroll
+            for (int p = 0; p < WPR; ++p) rmax = max(rmax, part_max[w0 + p]);
+            __syncthreads();
+            t = __fdiv_rn(bf16mag_to_f32(rmax), kNvfp4ScaleDivisor);
+            if (li == 0 && real) row_scale[r] = t;
+        } else if (real) {
+            t = __fdiv_rn(group_amax[r / rpg], kNvfp4ScaleDivisor);
+        }
+        if (!real) continue;
+        const float six_t = __fmul_rn(6.0f, t), four_t = __fmul_rn(4.0f, t);
+        uint2* crow = reinterpret_cast<uint2*>(codes + r * (K >> 1));
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            const int b = li + 32 * WPR * i;
+            if (b < nblk) {
+                uint2 c;
+                uint32_t s;
+                nvfp4_block<FOUR_SIX>(va[i], vb[i], bmax[i], t, six_t, four_t, c, s);
+                crow[b] = c;
+                store_sf(sf, SWZ, r, b, nblk, s);
+            } else if (SWZ && b < ncol_pad) {
+                store_sf(sf, SWZ, r, b, nblk, 0u);
+            }
+        }
+    }
+}
+
 // Long rows (K > 8192): two passes over the row, chunk by chunk.
 template <bool FOUR_SIX, bool SWZ, int TMODE>
 __global__ void __launch_bounds__(256) k_nvfp4_rows_long(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
@@ -723,10 +800,9 @@ static void launch_rows_t(const uint16_t* x, int64_t rows, int64_t K, int64_t ld
         k_nvfp4_rows<2, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 128)
         k_nvfp4_rows<4, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
-    else if (nblk <= 256)
-        k_nvfp4_rows<8, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 512)
-        k_nvfp4_rows<16, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
+        k_nvfp4_rows_wide<F46, SWZ, TM><<<grid_for(rows_iter * 4, sms), 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs,
+                                                                                     gam, rpg);
     else
         k_nvfp4_rows_long<F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
 }
