@@ -101,6 +101,53 @@ __global__ void __launch_bounds__(256) k_route_scan(int32_t* __restrict__ hist, 
     }
 }
 
+// Phase C, E <= RT_CTA_MAX_E: one CTA of 256 threads per chunk, two rounds of
+// 256 pairs.  In a round, pair i goes to thread i; lanes of a warp routed to
+// the same expert are ranked with __match_any_sync, the warps' per-expert
+// counts go to shared memory, and a pair's slot is its expert's running fill
+// + the counts of the earlier warps + its rank in the warp: the ascending
+// (token, k) order of the single-warp walk below, in one pass per round.
+constexpr int RT_CTA_MAX_E = 512;
+__global__ void __launch_bounds__(256) k_route_assign_cta(const int32_t* __restrict__ ids, int64_t n, int32_t E,
+                                                          const int32_t* __restrict__ hist,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ slot_of, int32_t* __restrict__ row_src)
+{
+    __shared__ int32_t fill[RT_CTA_MAX_E];
+    __shared__ int32_t cnt[8][RT_CTA_MAX_E];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += 256) fill[e] = offsets[e] + hist[(int64_t)blockIdx.x * E + e];
+    const int64_t i0 = (int64_t)blockIdx.x * RT_CHUNK, i1 = min(n, i0 + RT_CHUNK);
+    for (int64_t base = i0; base < i1; base += 256) {
+        for (int j = tid; j < 8 * E; j += 256) cnt[j / E][j % E] = 0;
+        __syncthreads();
+        const int64_t i = base + tid;
+        const bool valid = i < i1;
+        int32_t e = valid ? __ldg(ids + i) : -1;
+        if (e >= E) e = -1;
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) cnt[warp][e] = __popc(same);
+        __syncthreads();
+        int32_t slot = -1;
+        if (e >= 0) {
+            int32_t before = 0;
+            for (int w = 0; w < warp; ++w) before += cnt[w][e];
+            slot = fill[e] + before + rank;
+            row_src[slot] = (int32_t)i;
+        }
+        if (valid) slot_of[i] = slot;
+        __syncthreads();
+        for (int ee = tid; ee < E; ee += 256) {
+            int32_t tot = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) tot += cnt[w][ee];
+            fill[ee] += tot;
+        }
+        __syncthreads();
+    }
+}
+
 // Phase C: one warp per chunk walks its pairs in order, 32 at a time; lanes
 // routed to the same expert are ranked with __match_any_sync.
 __global__ void __launch_bounds__(32) k_route_assign(const int32_t* __restrict__ ids, int64_t n, int32_t E,
@@ -319,7 +366,9 @@ void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_
         cudaMemsetAsync(ticket, 0, sizeof(int32_t), st);
     }
     k_route_scan<<<E, 256, 0, st>>>(hist, nchunks, E, counts, offsets, ticket);
-    if (nchunks > 0)
+    if (nchunks > 0 && E <= RT_CTA_MAX_E)
+        k_route_assign_cta<<<nchunks, 256, 0, st>>>(ids, n, E, hist, offsets, slot_of, row_src);
+    else if (nchunks > 0)
         k_route_assign<<<nchunks, 32, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, offsets, slot_of, row_src);
 }
 
