@@ -167,3 +167,41 @@ def test_gemm_bad_offsets_reported(gpu, O):
                                 dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == gpu.DEV_BAD_OFFSETS
+
+
+def test_gemm_many_experts_offsets_in_global(gpu, O):
+    """More experts than the kernel caches in shared memory (its expert lookup
+    then reads the offsets from global memory)."""
+    counts = [(7 * e) % 40 for e in range(300)]
+    offsets, M, A, B = _make_problem(O, counts, 128, 128, seed=21)
+    out = _run(gpu, O, offsets, A, B, gpu.EPI_F32)
+    ref, ab = _reference(O, offsets, A, B)
+    _assert_close(to_np(out), ref, ab)
+
+
+@pytest.mark.parametrize("epilogue", ["f32", "bf16"])
+def test_gemm_capacity_not_tile_aligned(gpu, O, epilogue):
+    """Segment starts are multiples of 128 but the capacity (and the last
+    segment) ends mid-tile: rows past the capacity are neither read nor
+    written."""
+    counts, K, N = [100, 72], 320, 256
+    offsets, M, A, B = _make_problem(O, counts, K, N, seed=31)
+    cap = int(offsets[1]) + counts[1]                       # 200: ends inside the second tile
+    ac, asf, at = A
+    A2 = (ac[:cap], asf[:cap], at[:cap])
+    offsets2 = offsets.copy()
+    offsets2[-1] = cap
+    # the SF buffer still holds whole 128-row tiles (swizzled layout)
+    bc, bsf, bt = B
+    E = bc.shape[0]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    epi = gpu.EPI_F32 if epilogue == "f32" else gpu.EPI_BF16
+    out = gpu.grouped_expert_gemm_fp4(to_dev(A2[0]), to_dev(O.sf_to_swizzled(A2[1])), to_dev(A2[2]),
+                                      to_dev(offsets2), to_dev(bc), to_dev(O.sf_to_swizzled(bsf.reshape(E * N, -1))),
+                                      to_dev(bt), epilogue=epi, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert out.shape[0] == cap
+    ref, ab = _reference(O, offsets2, A2, B)
+    got = to_np(out) if epilogue == "f32" else synth.bf16_bits_to_f32(to_np(out))
+    _assert_close(got, ref, ab, extra=0.0 if epilogue == "f32" else 2.0 ** -8)

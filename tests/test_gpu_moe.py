@@ -290,3 +290,10 @@ def test_moe_deepseek_shaped_sampled(gpu, O):
     of = synth.bf16_bits_to_f32(out_gpu[s_t]).astype(np.float64)  # [tokens, k, H]: the sampled tokens only
     terms = np.abs(of * w_t[:, :, None]).sum(axis=1)
     assert np.all(np.abs(yg - yr) <= 2.0 ** -7 * np.abs(yr) + 1e-6 * terms + 1e-30)
+
+
+def test_moe_staged_many_experts(gpu, O):
+    """600 experts: the routing's single-warp slot assignment (beyond the
+    CTA version's expert limit) and the GEMM's offsets read from global
+    memory."""
+    _staged(gpu, O, T=160, H=256, I=128, E=600, k=3, four_six=False, seed=8)
