@@ -305,38 +305,20 @@ __global__ void k_group_finalize(float* __restrict__ scale, int64_t groups)
 // MXFP8 row + column copies.  CTA tile 128 rows x 128 columns, 512 threads.
 // Phase 1 (row copy): thread item = (row r, 16-byte chunk ch of 8 bf16), four
 // lanes per 32-element block, straight from registers; the tile also goes to
-// shared memory (256-byte rows, chunk ch of row r stored at ch ^ ((r >> 4) & 7)).
-// Phase 2 (column copy): thread = (column pair p, row group g): it reads
-// 16 bf16 pairs (columns 2p, 2p+1, rows 16g .. +15), one 32-bit word each; the
-// chunk permutation puts the 8 row groups of a warp on distinct banks.  An
-// MXFP8 block of a column (32 rows) is two row groups (block maximum with the
-// lane 4 away); each thread writes 16 contiguous bytes per column, so the 8
-// row groups of a column store 128 contiguous bytes.  The block scale bytes of
-// a row (phase 1) or of a column (phase 2) are gathered by shuffles into one
-// 32-bit store of 4 consecutive blocks where the layout allows it.
+// shared memory (256-byte rows, chunk ch of row r stored at
+// ch ^ (((r >> 3) & 3) << 2)).
+// Phase 2 (column copy): thread = (column quad q, row group g): it reads 8
+// rows of 4 columns (columns 4q .. 4q+3, rows 8g .. 8g+7) with 8-byte loads.
+// Warp w covers column quads 8 (w & 3) .. +7 and row groups 4 (w >> 2) .. +3,
+// i.e. one MXFP8 block (32 rows) of 32 columns: the block maxima are folded
+// over the 4 row groups by shuffles, and the permutation keeps the warp's 4
+// rows on distinct banks.  Each thread writes 8 contiguous code bytes per
+// column (32 contiguous bytes per block and column).  The block scale bytes
+// of the tile's rows and of its columns each go through a 512-byte shared
+// table and leave as one 32-bit word (4 consecutive blocks) per row or column.
 constexpr int MX_TILE = 128;
 
-BSQ_DEVICE int mx_chunk(int r, int ch) { return r * 16 + (ch ^ ((r >> 4) & 7)); }  // in 16-byte units
-
-// Block scale byte v of block `col` of SF row `row`; lanes `lane0`, lane0 +
-// stride, +2 stride, +3 stride hold blocks col0 .. col0+3 (col0 % 4 == 0).
-// All lanes call; the lane with `leader` set writes.
-BSQ_DEVICE void mx_store_sf4(uint8_t* sf, bool swz, int64_t row, int64_t col0, int64_t ncols, uint32_t v,
-                             int stride, bool leader, bool in_range)
-{
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, v, stride);
-    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, v, 2 * stride);
-    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, v, 3 * stride);
-    if (!leader || !in_range) return;
-    const uint32_t b[4] = {v & 0xFFu, b1 & 0xFFu, b2 & 0xFFu, b3 & 0xFFu};
-    if (swz || ((ncols & 3) == 0 && col0 + 4 <= ncols)) {
-        const int64_t off = swz ? sf_swizzled(row, col0, (ncols + 3) >> 2) : row * ncols + col0;
-        *reinterpret_cast<uint32_t*>(sf + off) = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-    } else {
-        for (int j = 0; j < 4; ++j)
-            if (col0 + j < ncols) sf[row * ncols + col0 + j] = (uint8_t)b[j];
-    }
-}
+BSQ_DEVICE int mx_chunk(int r, int ch) { return r * 16 + (ch ^ (((r >> 3) & 3) << 2)); }  // in 16-byte units
 
 template <bool SWZ, bool ROW, bool COL>
 __global__ void __launch_bounds__(512) k_mxfp8_rowcol(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
@@ -345,6 +327,7 @@ __global__ void __launch_bounds__(512) k_mxfp8_rowcol(const uint16_t* __restrict
                                                       uint8_t* __restrict__ col_sf)
 {
     __shared__ __align__(16) uint4 tile[MX_TILE * 16];
+    __shared__ uint8_t sfrow[MX_TILE][4];  // row scale bytes of the tile's 4 blocks per row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row0 = (int64_t)blockIdx.y * MX_TILE, col0 = (int64_t)blockIdx.x * MX_TILE;
     const int64_t nsf_row = K >> 5, nsf_col = rows >> 5;
@@ -384,60 +367,84 @@ __global__ void __launch_bounds__(512) k_mxfp8_rowcol(const uint16_t* __restrict
             }
             const bool ok = gr < rows && gc < K;
             if (ok) *reinterpret_cast<uint2*>(row_codes + gr * K + gc) = c;
-            // blocks of this row: chunk leaders ch = 0, 4, 8, 12 (lanes 4 apart)
-            mx_store_sf4(row_sf, SWZ, gr, col0 >> 5, nsf_row, s, 4, (ch & 15) == 0, gr < rows && col0 < K);
+            if ((ch & 3) == 0) sfrow[r][ch >> 2] = (uint8_t)s;
+        }
+    }
+    __syncthreads();
+    if (ROW && tid >= 512 - MX_TILE) {  // one word of 4 block scales per row of the tile
+        const int r = tid - (512 - MX_TILE);
+        const int64_t gr = row0 + r, cb = col0 >> 5;
+        if (gr < rows && col0 < K) {
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(sfrow[r]);
+            if (SWZ || ((nsf_row & 3) == 0 && cb + 4 <= nsf_row)) {
+                const int64_t o = SWZ ? sf_swizzled(gr, cb, (nsf_row + 3) >> 2) : gr * nsf_row + cb;
+                *reinterpret_cast<uint32_t*>(row_sf + o) = word;
+            } else {
+                for (int j = 0; j < 4; ++j)
+                    if (cb + j < nsf_row) row_sf[gr * nsf_row + cb + j] = (uint8_t)(word >> (8 * j));
+            }
         }
     }
     if (!COL) return;
+    __shared__ uint8_t sfcol[MX_TILE][4];  // column scale bytes of the tile's 4 blocks
+    const int cs = lane & 7, gs = lane >> 3;
+    const int q = 8 * (warp & 3) + cs;    // column quad: columns 4q .. 4q+3 of the tile
+    const int g = 4 * (warp >> 2) + gs;   // row group: rows 8g .. 8g+7
+    const int blk = warp >> 2;            // the tile's MXFP8 block these rows belong to
+    const uint8_t* tb = reinterpret_cast<const uint8_t*>(tile);
+    uint2 cv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * g + i;
+        cv[i] = *reinterpret_cast<const uint2*>(tb + 16 * mx_chunk(r, q >> 1) + 8 * (q & 1));
+    }
+    uint32_t m01 = 0u, m23 = 0u;  // bf16 magnitude maxima of columns (0, 1) and (2, 3)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m01 = absmax_bf16x2(m01, cv[i].x);
+        m23 = absmax_bf16x2(m23, cv[i].y);
+    }
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {  // the other 3 row groups of the block
+        m01 = __vmaxu2(m01, __shfl_xor_sync(0xFFFFFFFFu, m01, off));
+        m23 = __vmaxu2(m23, __shfl_xor_sync(0xFFFFFFFFu, m23, off));
+    }
+    const int64_t gr = row0 + 8 * g;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t mc = ((c < 2 ? m01 : m23) >> (16 * (c & 1))) & 0xFFFFu;
+        uint32_t w0 = 0u, w1 = 0u, sc = 0u;
+        if (mc) {
+            const int X = mx_exponent(mc << 16);
+            const float mul = mx_multiplier(X);
+            sc = (uint32_t)(X + 127);
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w = c < 2 ? cv[i].x : cv[i].y;
+                f[i] = __fmul_rn((c & 1) ? bf16_hi(w) : bf16_lo(w), mul);
+            }
+            w0 = e4m3x4(f[0], f[1], f[2], f[3]);
+            w1 = e4m3x4(f[4], f[5], f[6], f[7]);
+        }
+        const int64_t gc = col0 + 4 * q + c;
+        if (gc < K && gr < rows) *reinterpret_cast<uint2*>(col_codes + gc * rows + gr) = make_uint2(w0, w1);
+        if (gs == 0) sfcol[4 * q + c][blk] = (uint8_t)sc;
+    }
     __syncthreads();
-    const int p = (lane & 3) + 4 * warp;  // column pair: columns 2p, 2p+1 of the tile
-    const int g = lane >> 2;              // row group: rows 16g .. 16g+15
-    const int64_t gc = col0 + 2 * p, gr = row0 + 16 * g;
-    float a[16], b[16];
-    uint32_t ma = 0, mb = 0;
-    const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int r = 16 * g + i;
-        const uint32_t w = tw[4 * mx_chunk(r, p >> 2) + (p & 3)];
-        ma = max(ma, w & 0x7FFFu);
-        mb = max(mb, (w >> 16) & 0x7FFFu);
-        a[i] = __uint_as_float(w << 16);
-        b[i] = __uint_as_float(w & 0xFFFF0000u);
+    if (tid < MX_TILE) {  // one word of 4 block scales per column of the tile
+        const int64_t gc = col0 + tid, cb = row0 >> 5;
+        if (gc < K && row0 < rows) {
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(sfcol[tid]);
+            if (SWZ || ((nsf_col & 3) == 0 && cb + 4 <= nsf_col)) {
+                const int64_t o = SWZ ? sf_swizzled(gc, cb, (nsf_col + 3) >> 2) : gc * nsf_col + cb;
+                *reinterpret_cast<uint32_t*>(col_sf + o) = word;
+            } else {
+                for (int j = 0; j < 4; ++j)
+                    if (cb + j < nsf_col) col_sf[gc * nsf_col + cb + j] = (uint8_t)(word >> (8 * j));
+            }
+        }
     }
-    ma = max(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 4));  // the other half of the 32-row block
-    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 4));
-    uint32_t sa = 0, sb = 0;
-    uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
-    if (ma) {
-        const int X = mx_exponent(ma << 16);
-        const float mul = mx_multiplier(X);
-        sa = (uint32_t)(X + 127);
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = e4m3x4(__fmul_rn(a[4 * j], mul), __fmul_rn(a[4 * j + 1], mul), __fmul_rn(a[4 * j + 2], mul),
-                          __fmul_rn(a[4 * j + 3], mul));
-        oa = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    if (mb) {
-        const int X = mx_exponent(mb << 16);
-        const float mul = mx_multiplier(X);
-        sb = (uint32_t)(X + 127);
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = e4m3x4(__fmul_rn(b[4 * j], mul), __fmul_rn(b[4 * j + 1], mul), __fmul_rn(b[4 * j + 2], mul),
-                          __fmul_rn(b[4 * j + 3], mul));
-        ob = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    if (gr < rows) {
-        if (gc < K) *reinterpret_cast<uint4*>(col_codes + gc * rows + gr) = oa;
-        if (gc + 1 < K) *reinterpret_cast<uint4*>(col_codes + (gc + 1) * rows + gr) = ob;
-    }
-    // blocks of a column: row groups 0, 2, 4, 6 hold blocks 0..3 of the tile (lanes 8 apart)
-    mx_store_sf4(col_sf, SWZ, gc, row0 >> 5, nsf_col, sa, 8, g == 0, gc < K && row0 < rows);
-    mx_store_sf4(col_sf, SWZ, gc + 1, row0 >> 5, nsf_col, sb, 8, g == 0, gc + 1 < K && row0 < rows);
 }
 
 // Zero the padding of a swizzled SF buffer (rows and columns beyond the
