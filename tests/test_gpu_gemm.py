@@ -205,3 +205,80 @@ def test_gemm_capacity_not_tile_aligned(gpu, O, epilogue):
     ref, ab = _reference(O, offsets2, A2, B)
     got = to_np(out) if epilogue == "f32" else synth.bf16_bits_to_f32(to_np(out))
     _assert_close(got, ref, ab, extra=0.0 if epilogue == "f32" else 2.0 ** -8)
+
+
+# ---- many ragged experts: odd and even tile counts, empty experts, K tails
+# (K % 256 != 0), segments of one row, and all three epilogues.
+
+_RAGGED_CASES = [
+    # counts, K, N: odd and even tile counts, empty experts, K tails (K % 256 != 0)
+    ([300, 1, 0, 129, 385, 128, 256, 50], 320, 512),
+    ([1000, 3, 700], 2048, 256),
+    ([129] * 9, 576, 768),
+]
+
+
+@pytest.mark.parametrize("counts,K,N", _RAGGED_CASES)
+@pytest.mark.parametrize("epilogue", ["f32", "bf16"])
+def test_gemm_ragged_experts(gpu, O, counts, K, N, epilogue):
+    offsets, M, A, B = _make_problem(O, counts, K, N, seed=sum(counts) + N)
+    out = _run(gpu, O, offsets, A, B, gpu.EPI_F32 if epilogue == "f32" else gpu.EPI_BF16)
+    ref, ab = _reference(O, offsets, A, B)
+    got = to_np(out) if epilogue == "f32" else synth.bf16_bits_to_f32(to_np(out))
+    _assert_close(got, ref, ab, extra=0.0 if epilogue == "f32" else 2.0 ** -8)
+
+
+def test_gemm_swiglu_ragged_experts(gpu, O):
+    counts, K, I = [300, 1, 0, 129, 385, 50], 320, 384
+    offsets, M, A, B = _make_problem(O, counts, K, 2 * I, seed=77)
+    out = _run(gpu, O, offsets, A, B, gpu.EPI_SWIGLU_BF16)
+    ref, ab = _reference(O, offsets, A, B)
+    h = O.swiglu(ref)
+    g, u = ref[:, :I], ref[:, I:]
+    dg, du = REL_ABS * ab[:, :I], REL_ABS * ab[:, I:]
+    sg = g / (1 + np.exp(-g))
+    bound = 1.1 * np.abs(u) * dg + np.abs(sg) * du + 2.0 ** -8 * np.abs(h) + 1e-30
+    got = synth.bf16_bits_to_f32(to_np(out)).astype(np.float64)
+    valid = np.concatenate([np.arange(offsets[e], offsets[e] + counts[e]) for e in range(len(counts))])
+    err = np.abs(got[valid] - h[valid])
+    assert np.all(err <= bound[valid]), np.max(err / bound[valid])
+
+
+@pytest.mark.parametrize("epilogue", ["f32", "bf16"])
+def test_gemm_capacity_ends_mid_tile_after_full_tiles(gpu, O, epilogue):
+    """Three full tiles, then a last tile that ends at a capacity of 456 rows
+    (mid-tile): rows past the capacity are neither read nor written."""
+    counts, K, N = [300, 72], 320, 256
+    offsets, M, A, B = _make_problem(O, counts, K, N, seed=41)
+    cap = int(offsets[1]) + counts[1]
+    ac, asf, at = A
+    A2 = (ac[:cap], asf[:cap], at[:cap])
+    offsets2 = offsets.copy()
+    offsets2[-1] = cap
+    bc, bsf, bt = B
+    E = bc.shape[0]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    epi = gpu.EPI_F32 if epilogue == "f32" else gpu.EPI_BF16
+    out = gpu.grouped_expert_gemm_fp4(to_dev(A2[0]), to_dev(O.sf_to_swizzled(A2[1])), to_dev(A2[2]),
+                                      to_dev(offsets2), to_dev(bc), to_dev(O.sf_to_swizzled(bsf.reshape(E * N, -1))),
+                                      to_dev(bt), epilogue=epi, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert out.shape[0] == cap
+    ref, ab = _reference(O, offsets2, A2, B)
+    got = to_np(out) if epilogue == "f32" else synth.bf16_bits_to_f32(to_np(out))
+    _assert_close(got, ref, ab, extra=0.0 if epilogue == "f32" else 2.0 ** -8)
+
+
+def test_gemm_bad_offsets_reported_wide_n(gpu, O):
+    offsets, M, A, B = _make_problem(O, [256, 256], 256, 256, seed=5)
+    bad = offsets.copy()
+    bad[1] = 200
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ac, asf, at = A
+    bc, bsf, bt = B
+    gpu.grouped_expert_gemm_fp4(to_dev(ac), to_dev(O.sf_to_swizzled(asf)), to_dev(at), to_dev(bad), to_dev(bc),
+                                to_dev(O.sf_to_swizzled(bsf.reshape(-1, bsf.shape[-1]))), to_dev(bt),
+                                dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gpu.DEV_BAD_OFFSETS
