@@ -303,7 +303,7 @@ def run_ours(args, w, rank, world, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
 
-    def fwd():
+    def fwd(x=x, ids_d=ids_d, wts_d=wts_d, y=y):
         bsq.moe_expert_forward(x, ids_d, wts_d, wgu, wd, I, four_six=four_six, workspace=ws, y=y, dev_status=status)
 
     K, Wm = args.steps, args.warmup
@@ -379,30 +379,66 @@ def run_ours(args, w, rank, world, local):
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / P["hbm_gbs"], "traffic": None, "peak_source": P["source"]}
 
-    # end to end through the public API, host buffers copied inside the timed region
-    y_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    # End to end through the public API: every step's inputs are copied from
+    # pinned host memory and its output back to pinned host memory, all inside
+    # the timed region.  The copies run on their own streams into two buffer
+    # sets, so step i+1's upload and step i-1's download overlap step i's
+    # forward, as a serving pipeline runs them; events order each buffer's
+    # reuse after the work that read it.
+    main = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    xs, idss, wtss, ys = [x, torch.empty_like(x)], [ids_d, torch.empty_like(ids_d)], [wts_d, torch.empty_like(wts_d)], \
+        [y, torch.empty_like(y)]
+    y_host = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     Ke = max(3, min(K, 30))
 
-    def e2e_step():
-        x.copy_(x_host, non_blocking=True)
-        ids_d.copy_(ids_host, non_blocking=True)
-        wts_d.copy_(wts_host, non_blocking=True)
-        fwd()
-        y_host.copy_(y, non_blocking=True)
+    def e2e_steps(n):
+        in_done = [torch.cuda.Event() for _ in range(n)]
+        fwd_done = [torch.cuda.Event() for _ in range(n)]
+        out_done = [torch.cuda.Event() for _ in range(n)]
 
-    for _ in range(2):
-        e2e_step()
+        def upload(i):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(fwd_done[i - 2])  # the forward that read this buffer set is done
+                xs[b].copy_(x_host, non_blocking=True)
+                idss[b].copy_(ids_host, non_blocking=True)
+                wtss[b].copy_(wts_host, non_blocking=True)
+                in_done[i].record(s_in)
+
+        s_in.wait_stream(main)  # nothing is copied before the timed region starts
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            main.wait_event(in_done[i])
+            if i >= 2:
+                main.wait_event(out_done[i - 2])  # this output buffer's previous download is done
+            fwd(xs[b], idss[b], wtss[b], ys[b])
+            fwd_done[i].record(main)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(fwd_done[i])
+                y_host[b].copy_(ys[b], non_blocking=True)
+                out_done[i].record(s_out)
+        main.wait_event(out_done[n - 1])
+
+    e2e_steps(2)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(Ke):
-        e2e_step()
+    e2e_steps(Ke)
     e1.record()
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / Ke, world)
+    # every step saw the same inputs: the last download must equal the device forward's output
+    if not torch.equal(y_host[(Ke - 1) % 2], ys[(Ke - 1) % 2].cpu()):
+        raise RuntimeError("end-to-end output differs from the device forward's")
     e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
-           "h2d_bytes_per_step": T * H * 2 + ids.nbytes + wts.nbytes, "d2h_bytes_per_step": T * H * 2}
+           "h2d_bytes_per_step": T * H * 2 + ids.nbytes + wts.nbytes, "d2h_bytes_per_step": T * H * 2,
+           "copies": "double-buffered on two copy streams, overlapping the forwards"}
 
     components = {} if args.no_components else quantizer_components(bsq, synth, dev, P)
 
