@@ -53,9 +53,8 @@ void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_
                   int32_t* offsets, int32_t* slot_of, int32_t* row_src, int64_t capacity, int32_t* dev_status,
                   cudaStream_t st);
 void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of,
-                          uint8_t* codes, uint8_t* sf, float* scale, bool four_six, int sms, cudaStream_t st);
-void launch_pad_rows(const int32_t* row_src, const int32_t* offsets, int32_t E, int64_t H, uint8_t* sf, float* scale,
-                     int sms, cudaStream_t st);
+                          const int32_t* offsets, const int32_t* counts, int32_t E, uint8_t* codes, uint8_t* sf,
+                          float* scale, bool four_six, int sms, cudaStream_t st);
 void launch_combine(const uint16_t* out, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of, const float* w,
                     uint16_t* y, int sms, cudaStream_t st);
 

@@ -189,6 +189,8 @@ __global__ void __launch_bounds__(32) k_route_assign(const int32_t* __restrict__
 template <int BPL, bool FOUR_SIX, int WPR = 1>
 __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, int64_t T, int64_t H,
                                                        int32_t topk, const int32_t* __restrict__ slot_of,
+                                                       const int32_t* __restrict__ offsets,
+                                                       const int32_t* __restrict__ counts, int32_t E,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                        float* __restrict__ scale)
 {
@@ -198,6 +200,18 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
     const int part = warp % WPR, li = 32 * part + lane;
     const int nblk = (int)(H >> 4);
     const int64_t ncol_tiles = (nblk + 3) >> 2;
+    // The padding rows of every expert segment (from its last routed row up to
+    // the next 128-row boundary) get scale 0 and all-zero scale factors, so the
+    // GEMM's padding rows are exact zeros: one expert per CTA, one 4-byte
+    // scale-factor word per thread step.
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int64_t p0 = (int64_t)__ldg(offsets + e) + __ldg(counts + e), p1 = __ldg(offsets + e + 1);
+        for (int64_t i = threadIdx.x; i < (p1 - p0) * ncol_tiles; i += blockDim.x) {
+            const int64_t r = p0 + i / ncol_tiles, wd = i % ncol_tiles;
+            *reinterpret_cast<uint32_t*>(sf + sf_swizzled(r, 4 * wd, ncol_tiles)) = 0u;
+            if (wd == 0) scale[r] = 0.0f;
+        }
+    }
     // CTA-uniform loop (the shared-memory fold below synchronizes the CTA)
     for (int64_t t0 = (int64_t)blockIdx.x * TPC; t0 < T; t0 += (int64_t)gridDim.x * TPC) {
         const int64_t t = t0 + warp / WPR;
@@ -284,22 +298,6 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
     }
 }
 
-// Padding rows of the routed matrix get zero scales (their products vanish).
-__global__ void k_pad_rows(const int32_t* __restrict__ row_src, const int32_t* __restrict__ offsets, int32_t E,
-                           int64_t H, uint8_t* __restrict__ sf, float* __restrict__ scale)
-{
-    const int64_t total = __ldg(offsets + E);
-    const int nblk = (int)(H >> 4);
-    const int64_t ncol_tiles = (nblk + 3) >> 2;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < total; r += nwarps) {
-        if (__ldg(row_src + r) >= 0) continue;
-        if (lane == 0) scale[r] = 0.0f;
-        for (int b = lane; b < (int)(ncol_tiles * 4); b += 32) sf[sf_swizzled(r, b, ncol_tiles)] = 0;
-    }
-}
-
 // Combine: y[t] = sum_j w[t][j] * out[slot_of[t*k + j]], binary32 in
 // ascending j, rounded to bf16.  One warp per token, 8 columns per lane step.
 __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ out, int64_t T, int64_t H,
@@ -373,30 +371,25 @@ void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_
 }
 
 void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of,
-                          uint8_t* codes, uint8_t* sf, float* scale, bool four_six, int sms, cudaStream_t st)
+                          const int32_t* offsets, const int32_t* counts, int32_t E, uint8_t* codes, uint8_t* sf,
+                          float* scale, bool four_six, int sms, cudaStream_t st)
 {
     const int nblk = (int)(H >> 4);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 16));
 #define BSQ_QS(B)                                                                                                  \
     do {                                                                                                           \
-        if (four_six) k_quant_scatter<B, true><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);     \
-        else k_quant_scatter<B, false><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);            \
+        if (four_six) k_quant_scatter<B, true><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);     \
+        else k_quant_scatter<B, false><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);            \
     } while (0)
     if (nblk <= 32) BSQ_QS(1);
     else if (nblk <= 64) BSQ_QS(2);
     else if (nblk <= 128) BSQ_QS(4);
     else {  // wide rows: 4 warps per token, up to 4 blocks per lane (H <= 8192)
         const int grid4 = (int)std::max<int64_t>(1, std::min<int64_t>((T + 1) / 2, (int64_t)sms * 16));
-        if (four_six) k_quant_scatter<4, true, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);
-        else k_quant_scatter<4, false, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, codes, sf, scale);
+        if (four_six) k_quant_scatter<4, true, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);
+        else k_quant_scatter<4, false, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);
     }
 #undef BSQ_QS
-}
-
-void launch_pad_rows(const int32_t* row_src, const int32_t* offsets, int32_t E, int64_t H, uint8_t* sf, float* scale,
-                     int sms, cudaStream_t st)
-{
-    k_pad_rows<<<sms * 8, 256, 0, st>>>(row_src, offsets, E, H, sf, scale);
 }
 
 void launch_combine(const uint16_t* out, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of, const float* w,
