@@ -544,6 +544,15 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         uint32_t tc = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tc) {
             const TileInfo t = tile_info(tile);
+            const int row = t.m0 + 32 * q + lane;
+            const bool active = swiglu || part < 2 * t.n_halves;
+            // bf16 epilogue: the row's FP32 rescale t_tok * t_expert is loaded while
+            // the tile's MMAs run, since the first half is rescaled before the
+            // accumulator goes back (a load issued after the wait would hold up
+            // the hand-off).  The other epilogues load it after the hand-off.
+            const float s_early = (EPI == BSQ_EPI_BF16 && active && row < p.m_capacity)
+                                      ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e))
+                                      : 0.0f;
             const bool ok = mbar_wait(acc_full, tc & 1u, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
                 if (lane == 0) {
@@ -553,12 +562,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int row = t.m0 + 32 * q + lane;
-            const bool active = swiglu || part < 2 * t.n_halves;
             if constexpr (EPI == BSQ_EPI_BF16) {
-                // two rounds of 32 columns (only 32 accumulator words live at a
-                // time); the accumulator goes back after the second load
-                const float s = (active && row < p.m_capacity) ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e)) : 0.0f;
+                // Both 32-column halves come out of tensor memory before the
+                // accumulator is handed back (the first already packed to bf16,
+                // so at most 48 words are live); the staging and the stores,
+                // which may wait for the previous store to drain, come after.
+                const float s = s_early;
+                uint32_t pk[2][16];
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     uint32_t r[32];
@@ -571,16 +581,17 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(acc_empty);
                     }
-                    if (!active) continue;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[h2][j] = pack_bf16x2(__uint_as_float(r[2 * j]) * s, __uint_as_float(r[2 * j + 1]) * s);
+                }
+                if (!active) continue;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
                     stage_reuse(lane);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t* v = r + 8 * c;
-                        stage_put(stage_buf, lane, c, pack_bf16x2(__uint_as_float(v[0]) * s, __uint_as_float(v[1]) * s),
-                                  pack_bf16x2(__uint_as_float(v[2]) * s, __uint_as_float(v[3]) * s),
-                                  pack_bf16x2(__uint_as_float(v[4]) * s, __uint_as_float(v[5]) * s),
-                                  pack_bf16x2(__uint_as_float(v[6]) * s, __uint_as_float(v[7]) * s));
-                    }
+                    for (int c = 0; c < 4; ++c)
+                        stage_put(stage_buf, lane, c, pk[h2][4 * c], pk[h2][4 * c + 1], pk[h2][4 * c + 2], pk[h2][4 * c + 3]);
                     stage_store(stage_buf, lane, &tmOut, t.nt * 256 + 64 * part + 32 * h2, t.m0 + 32 * q);
                 }
                 continue;
