@@ -33,6 +33,18 @@ def test_nvfp4_per_token(gpu, O, rows, K, four_six, swz):
     _nvfp4_case(gpu, O, x, four_six, swz)
 
 
+@pytest.mark.parametrize("swz", [False, True])
+def test_nvfp4_four_six_tie(gpu, O, swz):
+    """Rows holding the block whose two 4/6 candidates tie in binary32 (the
+    oracle pin of the same name): the kernel keeps the 6-candidate too."""
+    from test_oracle_quant import four_six_tie_row
+    tie = four_six_tie_row()
+    x = synth.normal_with_outliers(96, 256, seed=5)
+    x[::3, :32] = tie
+    x[1::3, 224:] = tie
+    _nvfp4_case(gpu, O, x, True, swz)
+
+
 @pytest.mark.parametrize("four_six", [False, True])
 def test_nvfp4_boundary_rows(gpu, O, four_six):
     x = synth.special_rows(512)

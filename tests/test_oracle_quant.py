@@ -218,6 +218,46 @@ def test_four_six_brute_force(O):
     assert n_four > 50   # the second candidate does get used on N(0,1) data
 
 
+# A block with one outlier (28.5) among small values, in a row whose maximum
+# (50.75, in the first block) sets t = rn(50.75 / 2688).  The candidates' block
+# scales are 256 (the 6-candidate) and 384 (the 4-candidate).  Both encode
+# 28.5 as 6 x 4.8333335 = 29 and 4 x 7.25 = 29 in binary32, and every other
+# element as 0, so the binary32 error sums tie and the strict rule keeps the
+# 6-candidate.  In exact arithmetic, or with the multiply and the subtract
+# fused, 6 x 4.8333335 is 29.000001 and the 4-candidate would look better: the
+# case pins the per-operation rounding of the error sum.
+FOUR_SIX_TIE_BLOCK = [-0.6484375, -0.8046875, -1.078125, -0.6484375, -0.7578125, -0.91796875, -0.1845703125,
+                      -1.140625, 0.052978515625, 0.31640625, -0.498046875, -0.97265625, 28.5, 0.85546875,
+                      -0.052734375, 0.1572265625]
+
+
+def four_six_tie_row():
+    row = np.zeros(32, np.float32)
+    row[0] = 50.75
+    row[16:] = FOUR_SIX_TIE_BLOCK
+    bits = (row.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), row)  # exact in bf16
+    return bits
+
+
+def test_four_six_tie_keeps_the_six_candidate(O):
+    f = np.float32
+    x = four_six_tie_row()[None, :]
+    c46, s46, t = O.nvfp4_quantize_rows(x, four_six=True)
+    assert t[0] == f(50.75) / f(2688)
+    d6, d4 = f(256.0) * t[0], f(384.0) * t[0]        # E4M3 0x78 = 256, 0x7C = 384
+    # the outlier's reconstruction and error, binary32 step by step
+    assert f(6.0) * d6 == f(29.0) and f(4.0) * d4 == f(29.0)
+    assert np.float64(6.0) * np.float64(d6) != 29.0    # exact product: not a tie
+    blk = np.array(FOUR_SIX_TIE_BLOCK, np.float32)
+    cc6, ss6, sse6 = O.nvfp4_block_candidate(blk, t[0], 6.0)
+    cc4, ss4, sse4 = O.nvfp4_block_candidate(blk, t[0], 4.0)
+    assert (ss6, ss4) == (0x78, 0x7C)
+    assert sse6 == sse4
+    assert s46[0, 1] == 0x78
+    assert np.array_equal(unpack(c46[:, 8:16])[0], cc6)
+
+
 def test_mxfp8_against_torch_float8(O):
     x = synth.rows_log_uniform_std(64, 256, seed=2)
     rc, rs, cc, cs = O.mxfp8_quantize_rowcol(x)
