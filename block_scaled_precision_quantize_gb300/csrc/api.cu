@@ -2,6 +2,7 @@
 // launches on the caller's stream.  No device memory is allocated here and
 // no stream is synchronized.
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -18,6 +19,7 @@ struct DevInfo {
     int sms;
 };
 DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
 
 // The current device must be an sm_103 (GB300-class) part.
 bsq_status current_device(int* sms)
@@ -25,6 +27,7 @@ bsq_status current_device(int* sms)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BSQ_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return BSQ_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);  // threads may share a device
     DevInfo& d = g_dev[dev];
     if (!d.known) {
         int major = 0, minor = 0, n = 0;

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <stdint.h>
 
 #include "../../include/bsq.h"
@@ -42,6 +43,24 @@ BSQ_DEVICE float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); 
 BSQ_DEVICE uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
 BSQ_DEVICE uint32_t fold_halves(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
 BSQ_DEVICE float bf16mag_to_f32(uint32_t m16) { return __uint_as_float(m16 << 16); }
+
+// ---------------------------------------------------------------- host helpers
+// Kernel attributes (the dynamic shared-memory opt-in) belong to each device's
+// copy of the kernel: run `set` once per device of the calling thread, and
+// again after a failure.  `done` is a bit per device id (ids >= 64 always run
+// `set`).
+template <class F>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& done, F set)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0u;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    err = set();
+    if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return err;
+}
 
 // ---------------------------------------------------------------- E2M1
 // Eight binary32 values -> eight E2M1 codes packed in a word (element i in

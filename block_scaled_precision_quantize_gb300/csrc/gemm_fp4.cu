@@ -681,14 +681,15 @@ static bool make_tmap(CUtensorMap* tm, const void* base, CUtensorMapDataType dt,
 
 cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t aerr = once_per_device(attr_done, [] {
         for (auto fn : {k_gemm_fp4<BSQ_EPI_F32>, k_gemm_fp4<BSQ_EPI_BF16>, k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>}) {
             cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM_BYTES);
             if (err != cudaSuccess) return err;
         }
-        attr_set = true;
-    }
+        return cudaSuccess;
+    });
+    if (aerr != cudaSuccess) return aerr;
     const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16;
     const int64_t kb = a.K / 2;          // bytes per row of codes
     const int64_t k64 = a.K / 64;        // SF chunks per row tile

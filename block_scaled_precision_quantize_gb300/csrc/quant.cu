@@ -867,13 +867,12 @@ static cudaError_t requant_main(dim3 grid, const uint8_t* codes, const uint8_t* 
                                 int64_t rows, int64_t K, const unsigned int* colmax, uint8_t* nvc, uint8_t* nvs,
                                 float* nvt, uint8_t* mxc, uint8_t* mxs, uint64_t seed, cudaStream_t st)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(k_requant_main<S, R, N, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)RQ_SMEM);
-        if (err != cudaSuccess) return err;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t err = once_per_device(attr_done, [] {
+        return cudaFuncSetAttribute(k_requant_main<S, R, N, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)RQ_SMEM);
+    });
+    if (err != cudaSuccess) return err;
     k_requant_main<S, R, N, M><<<grid, 256, RQ_SMEM, st>>>(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc,
                                                             mxs, philox_keys(seed));
     return cudaGetLastError();
