@@ -220,35 +220,37 @@ BSQ_DEVICE uint32_t sr_pick16(uint4 w, int i)
 // |v| >= max saturates.  Where the grid spacing is the binary32 spacing of
 // |v| shifted by s bits (the normal ranges), (|v| - lo) / (hi - lo) * 65536
 // equals (the s dropped bits) / 2^(s-16), so "round up" is a carry out of
-// those bits after adding 2^s - 1 - (r << (s-16)); below the normal range the
-// comparison is made in binary32, where every step is exact.
+// those bits after adding 2^s - 1 - (r << (s-16)).  Below the normal range the grid is uniform, g * 2^-s' (E2M1: 0.5 below 1;
+// E4M3: 2^-9 below 2^-6), and X = |v| * 2^(s'+16) is exact.  With
+// C = ceil(X) = 65536 k + c: rounding up iff r < f * 65536 (f the fraction of
+// |v| / 2^-s') is, for an integer r, the carry out of c + 65535 - r, so the
+// code is (C + 65535 - r) >> 16.  Both formulas can only overshoot the
+// largest finite code from above, so saturation is a min.
+BSQ_DEVICE uint32_t sr_uniform_code(float a, float scale_2p, uint32_t r16)
+{
+    uint32_t c;
+    asm("cvt.rpi.u32.f32 %0, %1;" : "=r"(c) : "f"(__fmul_rn(a, scale_2p)));
+    return (c + (0xFFFFu - r16)) >> 16;
+}
 BSQ_DEVICE uint32_t e2m1_sr(float v, uint32_t r16)
 {
-    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    const float a = fabsf(v);
+    const uint32_t bits = __float_as_uint(v), abits = bits & 0x7FFFFFFFu;
     // [1, 6): one mantissa bit kept (codes 2 .. 7 from the binary32 exponent and top bit)
-    uint32_t code = ((__float_as_uint(a) + (0x3FFFFFu - (r16 << 6))) >> 22) - 252u;
-    if (a < 1.0f) {  // grid 0, 0.5, 1 (codes 0, 1, 2)
-        const float y = __fmul_rn(a, 2.0f);
-        const float m = truncf(y);
-        code = (uint32_t)m + (((float)r16 < __fmul_rn(__fsub_rn(y, m), 65536.0f)) ? 1u : 0u);
-    }
-    if (a >= 6.0f) code = 7u;
-    return sign | code;
+    const uint32_t normal = ((abits + (0x3FFFFFu - (r16 << 6))) >> 22) - 252u;
+    // [0, 1): grid 0.5 (codes 0, 1, 2), X = |v| * 2^17
+    const uint32_t low = sr_uniform_code(__uint_as_float(abits), 131072.0f, r16);
+    const uint32_t code = min(abits < 0x3F800000u ? low : normal, 7u);
+    return ((bits >> 28) & 8u) | code;
 }
 BSQ_DEVICE uint32_t e4m3_sr(float v, uint32_t r16)
 {
-    const uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
-    const float a = fabsf(v);
+    const uint32_t bits = __float_as_uint(v), abits = bits & 0x7FFFFFFFu;
     // normal range [2^-6, 448): three mantissa bits kept; code = ((e - 120) << 3) | m
-    uint32_t code = ((__float_as_uint(a) + (0xFFFFFu - (r16 << 4))) >> 20) - 960u;
-    if (a < 0.015625f) {  // subnormal grid m * 2^-9
-        const float y = __fmul_rn(a, 512.0f);
-        const float m = truncf(y);
-        code = (uint32_t)m + (((float)r16 < __fmul_rn(__fsub_rn(y, m), 65536.0f)) ? 1u : 0u);
-    }
-    if (a >= 448.0f) code = 0x7Eu;
-    return sign | code;
+    const uint32_t normal = ((abits + (0xFFFFFu - (r16 << 4))) >> 20) - 960u;
+    // [0, 2^-6): grid 2^-9 (codes 0 .. 8), X = |v| * 2^25
+    const uint32_t low = sr_uniform_code(__uint_as_float(abits), 33554432.0f, r16);
+    const uint32_t code = min(abits < 0x3C800000u ? low : normal, 0x7Eu);
+    return ((bits >> 24) & 0x80u) | code;
 }
 
 // ---------------------------------------------------------------- NVFP4 block

@@ -75,6 +75,35 @@ def test_stochastic_encoders(gpu, O, kind):
     assert bits_equal(got[idx], ref), first_mismatch(got[idx], ref)
 
 
+def _sr_boundary_cases(grid):
+    """Values lo + (j / 65536) * (hi - lo) inside every grid interval, j at the
+    carry boundaries, each with random bits j - 1, j and j + 1: rounding up is
+    decided exactly at r = j."""
+    vals, bits = [], []
+    for lo, hi in zip(grid[:-1], grid[1:]):
+        for j in (1, 2, 255, 256, 32767, 32768, 65535):
+            v = np.float32(lo + (hi - lo) * (j / 65536.0))
+            assert float(v) == lo + (hi - lo) * (j / 65536.0)      # exact in binary32
+            for r in (j - 1, j, j + 1):
+                if 0 <= r < 65536:
+                    vals += [v, -v]
+                    bits += [r, r]
+    return np.array(vals, np.float32), np.array(bits, np.uint32)
+
+
+@pytest.mark.parametrize("kind", [2, 3])
+def test_stochastic_encoders_carry_boundaries(gpu, O, kind):
+    if kind == 2:
+        grid = [0, .5, 1, 1.5, 2, 3, 4, 6]
+    else:
+        grid = sorted({O.e4m3_decode(c) for c in range(0x7F)})   # 0 .. 448, subnormals included
+    v, r = _sr_boundary_cases([float(g) for g in grid])
+    got = to_np(gpu.format_probe(kind, to_dev(v), to_dev(r)))
+    enc = O.e2m1_encode_sr if kind == 2 else O.e4m3_encode_sr
+    ref = np.array([enc(float(a), int(b)) for a, b in zip(v, r)], np.uint8)
+    assert bits_equal(got, ref), first_mismatch(got, ref)
+
+
 def test_philox_bits_match_oracle(gpu, O):
     for seed, stream, idx0 in [(7, 0, 0), (7, 1, 0), (0xDEADBEEFCAFEF00D, 1, (1 << 35) - 13), (123, 0, 999)]:
         n = 4096
