@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                        float* __restrict__ scale)
 {
-    constexpr int TPC = 8 / WPR;  // tokens per CTA step
+    const int TPC = (int)(blockDim.x >> 5) / WPR;  // tokens per CTA step (one per WPR warps)
     __shared__ uint32_t part_max[8];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int part = warp % WPR, li = 32 * part + lane;
@@ -375,11 +375,15 @@ void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk,
                           float* scale, bool four_six, int sms, cudaStream_t st)
 {
     const int nblk = (int)(H >> 4);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 16));
+    // one warp per token in CTAs of 4 warps: at ~70 registers a thread, an SM
+    // holds 7 such CTAs (28 warps) against 3 CTAs of 8 warps (24)
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 3) / 4, (int64_t)sms * 32));
 #define BSQ_QS(B)                                                                                                  \
     do {                                                                                                           \
-        if (four_six) k_quant_scatter<B, true><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);     \
-        else k_quant_scatter<B, false><<<grid, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);            \
+        if (four_six)                                                                                              \
+            k_quant_scatter<B, true><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale); \
+        else                                                                                                       \
+            k_quant_scatter<B, false><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale); \
     } while (0)
     if (nblk <= 32) BSQ_QS(1);
     else if (nblk <= 64) BSQ_QS(2);

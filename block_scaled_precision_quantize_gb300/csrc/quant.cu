@@ -805,8 +805,8 @@ static void launch_rows_t(const uint16_t* x, int64_t rows, int64_t K, int64_t ld
         k_nvfp4_rows<1, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 64)
         k_nvfp4_rows<2, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
-    else if (nblk <= 128)
-        k_nvfp4_rows<4, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
+    else if (nblk <= 128)  // ~70 registers a thread: CTAs of 4 warps fill an SM (28 warps) better than of 8 (24)
+        k_nvfp4_rows<4, F46, SWZ, TM><<<2 * grid, 128, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 512)
         k_nvfp4_rows_wide<F46, SWZ, TM><<<grid_for(rows_iter * 4, sms), 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs,
                                                                                      gam, rpg);
