@@ -27,22 +27,22 @@
 //   warp 1      allocates tensor memory; one lane issues one 128 x 256 x 64
 //               MMA per K step and the commits.  It touches shared memory only
 //               for its barrier waits (a tile's width is all it needs to know)
-//   warps 2-5   one per tensor-memory lane quadrant: as soon as a stage's
-//               scale factors land, copy them into tensor memory with
-//               tcgen05.st while the codes are still in flight.  B's chunks are
-//               replicated in every quadrant (the layout tcgen05.cp
-//               32x128b.warpx4 produces); for A, the lanes of quadrant q read
-//               only column q of each 4-column chunk group (rows 32q + l), so
-//               one 4-byte word per chunk row is enough
-//   warps 6-21  epilogue, four warps per lane quadrant, 64 columns each: load
+//   warps 2-4   as soon as a stage's scale factors land, one lane each
+//               copies a third of them into tensor memory with tcgen05.cp
+//               32x128b.warpx4 while the codes are still in flight (each
+//               512-byte chunk lands replicated in all four lane quadrants)
+//   warps 5-20  epilogue, four warps per lane quadrant, 64 columns each: load
 //               the accumulator, hand it back to the MMA warp, then rescale /
 //               SwiGLU / store while the next tile's MMAs run
-// Shared memory: GM_STAGES stages of [SFA 2 KB][SFB 4 KB][A 16 KB][B 32 KB]
-// (A and B 128-byte swizzled, 1024-byte aligned), the expert offsets, and a
-// 2 KB staging buffer per epilogue warp.  A warp holds 32 output rows (one per
-// thread); for bf16 outputs it writes each 32 x 32 block into its buffer and
-// one lane stores it with a TMA tensor store: one global store instruction
-// per 2 KB instead of 128 scattered 16-byte stores.
+// Shared memory: a ring of stages of [SFA 2 KB][SFB 4 KB][A 16 KB][B 32 KB]
+// (A and B 128-byte swizzled, 1024-byte aligned) and the expert offsets.  The
+// ring's depth is what hides the round trip of a stage (MMAs complete ->
+// stage released -> copies issued -> copies landed: ~2700 cycles against 512
+// cycles of MMAs per stage), so every epilogue that can store straight from
+// registers gets four stages.  Only the plain bf16 epilogue, whose 128 x 256
+// output tile is the largest, keeps three stages plus a 2 KB staging buffer
+// per epilogue warp: a warp writes each 32 x 32 block of its 32 rows there
+// and one lane stores it with a TMA tensor store.
 // Tensor memory: 512 columns = accumulator (256) + an SF ring (48 per stage:
 // SFA k-step j at 4j, SFB k-step j at 16 + 8j, both N halves side by side).
 // Every mbarrier wait is bounded; on expiry the CTA records BSQ_DEV_TIMEOUT,
@@ -58,7 +58,7 @@ namespace bsq {
 constexpr int GM_SF_WARPS = 3;
 constexpr int GM_EPI_WARPS = 16;
 constexpr int GM_THREADS = 32 * (2 + GM_SF_WARPS + GM_EPI_WARPS);  // 672
-constexpr int GM_STAGES = 3;
+constexpr int GM_MAX_STAGES = 4;
 constexpr int GM_SFA_OFF = 0;
 constexpr int GM_SFB_OFF = 2048;
 constexpr int GM_A_OFF = 6144;
@@ -69,9 +69,20 @@ constexpr int GM_SF_RING = 256;                       // first SF column
 constexpr int GM_SF_STAGE_COLS = 48;
 constexpr int GM_MAX_SMEM_EXPERTS = 256;              // offsets cached in shared memory up to this E
 constexpr uint32_t GM_SPIN_LIMIT = 1u << 22;
-constexpr int GM_EPI_OFF = GM_STAGES * GM_STAGE_BYTES;        // epilogue staging, per warp
 constexpr int GM_EPI_WARP_BYTES = 32 * 64;                     // 32 rows x 64 bytes, 64-byte swizzled
-constexpr size_t GM_SMEM_BYTES = (size_t)GM_EPI_OFF + (size_t)GM_EPI_WARPS * GM_EPI_WARP_BYTES + 1024;
+
+// Per epilogue kind: the stage count, whether the epilogue stages its stores
+// through shared memory (after the ring), and the dynamic shared memory.
+template <int EPI>
+struct GmCfg {
+    static constexpr bool STAGED = EPI == BSQ_EPI_BF16;
+    static constexpr int STAGES = STAGED ? 3 : 4;
+    static constexpr int EPI_OFF = STAGES * GM_STAGE_BYTES;
+    static constexpr size_t SMEM_BYTES =
+        (size_t)EPI_OFF + (STAGED ? (size_t)GM_EPI_WARPS * GM_EPI_WARP_BYTES : 0) + 1024;
+};
+static_assert(GM_SF_RING + GM_MAX_STAGES * GM_SF_STAGE_COLS <= GM_TMEM_COLS, "SF ring exceeds tensor memory");
+static_assert(GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES + 2048 <= 232448, "stage ring exceeds shared memory");
 
 // Instruction descriptors, kind::mxf4nvf4: A and B are E2M1 (format 1),
 // K-major, no negation, N>>3 at bit 17, M = 128 (M>>4 at bit 24), scale type
@@ -276,6 +287,22 @@ BSQ_DEVICE void stage_reuse(int lane)
     __syncwarp();
 }
 
+// 32 bytes of one output row straight from registers: one 256-bit store (a
+// whole 32-byte sector per lane) when the destination is 32-byte aligned, else
+// two 128-bit stores.
+BSQ_DEVICE void st_row32(void* ptr, const uint32_t* w, bool vec32)
+{
+    if (vec32) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else {
+        uint4* q = static_cast<uint4*>(ptr);
+        q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 struct GemmParams {
     const uint8_t* a_sf;
@@ -292,6 +319,7 @@ struct GemmParams {
     int32_t N;
     int32_t n_tiles;
     int32_t epilogue;
+    bool out_vec32;  // output base and row pitch are 32-byte aligned
 };
 
 struct TileInfo {
@@ -306,8 +334,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmOut,
                const GemmParams p)
 {
+    constexpr int GM_STAGES = GmCfg<EPI>::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[4 * GM_STAGES + 3 + GM_SF_WARPS];
+    __shared__ __align__(8) uint64_t bars[4 * GM_MAX_STAGES + 3 + GM_SF_WARPS];
     __shared__ int32_t s_off[GM_MAX_SMEM_EXPERTS + 1];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort, s_bad;
@@ -540,7 +569,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int q = warp & 3;                                  // tensor-memory lane quadrant
         const int part = (warp - 2 - GM_SF_WARPS) >> 2;          // 0..3: which 64 columns (32 h for SwiGLU)
         const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
-        uint8_t* stage_buf = smem + GM_EPI_OFF + (warp - 2 - GM_SF_WARPS) * GM_EPI_WARP_BYTES;
+        uint8_t* stage_buf = smem + GmCfg<EPI>::EPI_OFF + (warp - 2 - GM_SF_WARPS) * GM_EPI_WARP_BYTES;
         uint32_t tc = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tc) {
             const TileInfo t = tile_info(tile);
@@ -613,19 +642,19 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             if (!active) continue;
             const float s = (row < p.m_capacity) ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e)) : 0.0f;
             if constexpr (swiglu) {
-                stage_reuse(lane);
+                // 32 h values = 64 contiguous bytes of this thread's row, stored
+                // from registers as two 32-byte sectors (or four 16-byte pieces
+                // when the output is only 16-byte aligned)
+                if (row < p.m_capacity) {
+                    uint32_t w[16];
 #pragma unroll
-                for (int c = 0; c < 32; c += 8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int g = c + 2 * j;
-                        w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[g]) * s, __uint_as_float(r[32 + g]) * s),
-                                           swiglu1(__uint_as_float(r[g + 1]) * s, __uint_as_float(r[33 + g]) * s));
-                    }
-                    stage_put(stage_buf, lane, c >> 3, w[0], w[1], w[2], w[3]);
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[2 * j]) * s, __uint_as_float(r[32 + 2 * j]) * s),
+                                           swiglu1(__uint_as_float(r[2 * j + 1]) * s, __uint_as_float(r[33 + 2 * j]) * s));
+                    uint8_t* d = static_cast<uint8_t*>(p.out) + ((size_t)row * p.ldo + t.nt * 128 + 32 * part) * 2;
+                    st_row32(d, w, p.out_vec32);
+                    st_row32(d + 32, w + 8, p.out_vec32);
                 }
-                stage_store(stage_buf, lane, &tmOut, t.nt * 128 + 32 * part, t.m0 + 32 * q);
             } else if (row < p.m_capacity) {
                 float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (size_t)row * p.ldo + t.nt * 256 +
                                                       64 * part);
@@ -635,8 +664,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                                        __uint_as_float(r[4 * i + 2]) * s, __uint_as_float(r[4 * i + 3]) * s);
             }
         }
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        __syncwarp();
+        if constexpr (GmCfg<EPI>::STAGED) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
@@ -683,11 +714,15 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
 {
     static std::atomic<uint64_t> attr_done{0};
     cudaError_t aerr = once_per_device(attr_done, [] {
-        for (auto fn : {k_gemm_fp4<BSQ_EPI_F32>, k_gemm_fp4<BSQ_EPI_BF16>, k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>}) {
-            cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM_BYTES);
-            if (err != cudaSuccess) return err;
-        }
-        return cudaSuccess;
+        cudaError_t err = cudaFuncSetAttribute(k_gemm_fp4<BSQ_EPI_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)GmCfg<BSQ_EPI_F32>::SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(k_gemm_fp4<BSQ_EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)GmCfg<BSQ_EPI_BF16>::SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES);
+        return err;
     });
     if (aerr != cudaSuccess) return aerr;
     const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16;
@@ -730,11 +765,11 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
             return cudaErrorInvalidValue;
     }
     CUtensorMap tmOut;
-    if (a.epilogue == BSQ_EPI_F32) {
-        memset(&tmOut, 0, sizeof(tmOut));  // f32 output is stored directly
+    if (a.epilogue != BSQ_EPI_BF16) {
+        memset(&tmOut, 0, sizeof(tmOut));  // f32 and SwiGLU outputs are stored from registers
     } else {
-        // bf16 output [m_capacity][ncols] with row pitch ldo: 32 x 32 boxes, 64-byte swizzle
-        const int64_t ncols = swiglu ? a.N / 2 : a.N;
+        // bf16 output [m_capacity][N] with row pitch ldo: 32 x 32 boxes, 64-byte swizzle
+        const int64_t ncols = a.N;
         const cuuint64_t d[2] = {(cuuint64_t)ncols, (cuuint64_t)a.m_capacity};
         const cuuint64_t s[1] = {(cuuint64_t)(a.ldo * 2)};
         const cuuint32_t b[2] = {32u, 32u};
@@ -755,14 +790,21 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
     p.K = (int32_t)a.K;
     p.N = (int32_t)a.N;
     p.epilogue = a.epilogue;
+    p.out_vec32 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0) && ((a.ldo * 2) % 32 == 0);
     p.n_tiles = swiglu ? (int32_t)(a.N / 256) : (int32_t)((a.N + 255) / 256);
     // persistent: at most one CTA per SM, never more CTAs than the largest possible tile count
     const int64_t max_tiles = ((a.m_capacity + 127) / 128) * p.n_tiles;
     const int64_t grid = std::min<int64_t>(max_tiles, a.sms);
     if (grid <= 0) return cudaSuccess;
-    auto kern = swiglu ? k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>
-                       : (a.epilogue == BSQ_EPI_BF16 ? k_gemm_fp4<BSQ_EPI_BF16> : k_gemm_fp4<BSQ_EPI_F32>);
-    kern<<<(unsigned)grid, GM_THREADS, GM_SMEM_BYTES, st>>>(tmA, tmB, tmSFB, tmOut, p);
+    if (swiglu)
+        k_gemm_fp4<BSQ_EPI_SWIGLU_BF16><<<(unsigned)grid, GM_THREADS, GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES, st>>>(
+            tmA, tmB, tmSFB, tmOut, p);
+    else if (a.epilogue == BSQ_EPI_BF16)
+        k_gemm_fp4<BSQ_EPI_BF16><<<(unsigned)grid, GM_THREADS, GmCfg<BSQ_EPI_BF16>::SMEM_BYTES, st>>>(tmA, tmB, tmSFB,
+                                                                                                     tmOut, p);
+    else
+        k_gemm_fp4<BSQ_EPI_F32><<<(unsigned)grid, GM_THREADS, GmCfg<BSQ_EPI_F32>::SMEM_BYTES, st>>>(tmA, tmB, tmSFB,
+                                                                                                   tmOut, p);
     return cudaGetLastError();
 }
 
