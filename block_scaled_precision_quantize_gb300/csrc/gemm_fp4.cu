@@ -27,11 +27,12 @@
 //   warp 1      allocates tensor memory; one lane issues one 128 x 256 x 64
 //               MMA per K step and the commits.  It touches shared memory only
 //               for its barrier waits (a tile's width is all it needs to know)
-//   warps 2-4   as soon as a stage's scale factors land, one lane each
-//               copies a third of them into tensor memory with tcgen05.cp
-//               32x128b.warpx4 while the codes are still in flight (each
-//               512-byte chunk lands replicated in all four lane quadrants)
-//   warps 5-20  epilogue, four warps per lane quadrant, 64 columns each: load
+//   warps 2..   one or three scale-factor movers: as soon as a stage's scale
+//               factors land, they are copied into tensor memory with
+//               tcgen05.cp 32x128b.warpx4 while the codes are still in flight
+//               (each 512-byte chunk lands replicated in all four lane
+//               quadrants)
+//   the last 16 warps  epilogue, four per lane quadrant, 64 columns each: load
 //               the accumulator, hand it back to the MMA warp, then rescale /
 //               SwiGLU / store while the next tile's MMAs run
 // Shared memory: a ring of stages of [SFA 2 KB][SFB 4 KB][A 16 KB][B 32 KB]
@@ -55,9 +56,8 @@
 
 namespace bsq {
 
-constexpr int GM_SF_WARPS = 3;
+constexpr int GM_MAX_SF_WARPS = 3;
 constexpr int GM_EPI_WARPS = 16;
-constexpr int GM_THREADS = 32 * (2 + GM_SF_WARPS + GM_EPI_WARPS);  // 672
 constexpr int GM_MAX_STAGES = 4;
 constexpr int GM_SFA_OFF = 0;
 constexpr int GM_SFB_OFF = 2048;
@@ -72,9 +72,17 @@ constexpr uint32_t GM_SPIN_LIMIT = 1u << 22;
 constexpr int GM_EPI_WARP_BYTES = 32 * 64;                     // 32 rows x 64 bytes, 64-byte swizzled
 
 // Per epilogue kind: the stage count, whether the epilogue stages its stores
-// through shared memory (after the ring), and the dynamic shared memory.
+// through shared memory (after the ring), the dynamic shared memory, and the
+// number of scale-factor mover warps.  Three movers (one chunk run each) get
+// each stage's scale factors into tensor memory soonest, which the four-stage
+// SwiGLU GEMM, bound by the stage round trip, needs; one mover keeps the CTA
+// at 19 warps, at most five per SM sub-partition and 96 registers a thread,
+// which lets the epilogue warps that share a sub-partition with the producer
+// hand the accumulator back in time on the short-K bf16 GEMM.
 template <int EPI>
 struct GmCfg {
+    static constexpr int SF_WARPS = EPI == BSQ_EPI_SWIGLU_BF16 ? 3 : 1;
+    static constexpr int THREADS = 32 * (2 + SF_WARPS + GM_EPI_WARPS);
     static constexpr bool STAGED = EPI == BSQ_EPI_BF16;
     static constexpr int STAGES = STAGED ? 3 : 4;
     static constexpr int EPI_OFF = STAGES * GM_STAGE_BYTES;
@@ -329,14 +337,15 @@ struct TileInfo {
 // EPI is the epilogue (BSQ_EPI_*): one instantiation per epilogue keeps each
 // one's register allocation to its own path.
 template <int EPI>
-__global__ void __launch_bounds__(GM_THREADS, 1)
+__global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
     k_gemm_fp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmOut,
                const GemmParams p)
 {
     constexpr int GM_STAGES = GmCfg<EPI>::STAGES;
+    constexpr int GM_SF_WARPS = GmCfg<EPI>::SF_WARPS;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[4 * GM_MAX_STAGES + 3 + GM_SF_WARPS];
+    __shared__ __align__(8) uint64_t bars[4 * GM_MAX_STAGES + 3 + GM_MAX_SF_WARPS];
     __shared__ int32_t s_off[GM_MAX_SMEM_EXPERTS + 1];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort, s_bad;
@@ -524,16 +533,18 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         __syncwarp();
     } else if (warp < 2 + GM_SF_WARPS) {
         // ------------------------------------------------------ scale factors -> tensor memory
-        // One lane of each of these three warps moves a third of a stage's
-        // scale factors into the tensor-memory ring with tcgen05.cp
-        // 32x128b.warpx4 (each 512-byte chunk lands in all four lane
-        // quadrants, the layout the block-scaled MMA reads): warp 2 A's four
-        // chunks (columns 4j), warps 3 and 4 B's first and second 128 rows
-        // (columns 16 + 8j and 20 + 8j), then commits them to the stage's SF
-        // barrier.  The copies start as soon as the SF land, while the codes
-        // are still in flight, and they neither pass through registers nor
-        // cost shared-memory reads beyond the 6 KB themselves.
-        const int which = warp - 2;  // 0: A, 1: B rows 0-127, 2: B rows 128-255
+        // A stage's scale factors go into the tensor-memory ring with
+        // tcgen05.cp 32x128b.warpx4 (each 512-byte chunk lands in all four
+        // lane quadrants, the layout the block-scaled MMA reads) in three
+        // chunk runs: A's four chunks (columns 4j), B's first and second 128
+        // rows (columns 16 + 8j and 20 + 8j).  With three mover warps, lane 0
+        // of warp 2 + r moves run r; with one, lane 0 of warp 2 moves all
+        // three.  Each then commits to the stage's SF barrier.  The copies
+        // start as soon as the SF land, while the codes are still in flight,
+        // and they neither pass through registers nor cost shared-memory
+        // reads beyond the 6 KB themselves.
+        const int w_sf = warp - 2;
+        const int run0 = GM_SF_WARPS == 1 ? 0 : w_sf, run1 = GM_SF_WARPS == 1 ? 3 : w_sf + 1;
         if (lane == 0) {
             uint32_t it = 0;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
@@ -548,20 +559,22 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t src = sbase + (uint32_t)s * GM_STAGE_BYTES +
-                                         (which == 0 ? GM_SFA_OFF : GM_SFB_OFF + 2048 * (which - 1));
-                    const uint32_t dst = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS +
-                                         (which == 0 ? 0u : 16u + 4u * (uint32_t)(which - 1));
-                    const uint32_t step = which == 0 ? 4u : 8u;
+                    for (int run = run0; run < run1; ++run) {
+                        const uint32_t src = sbase + (uint32_t)s * GM_STAGE_BYTES +
+                                             (run == 0 ? GM_SFA_OFF : GM_SFB_OFF + 2048 * (run - 1));
+                        const uint32_t dst = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS +
+                                             (run == 0 ? 0u : 16u + 4u * (uint32_t)(run - 1));
+                        const uint32_t step = run == 0 ? 4u : 8u;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tc_cp_sf(dst + step * j, smem_desc(src + 512 * j, 16, 128, 0));
+                        for (int j = 0; j < 4; ++j) tc_cp_sf(dst + step * j, smem_desc(src + 512 * j, 16, 128, 0));
+                    }
                     tc_commit(sf_bar(s));
                 }
             }
             // every copy issued here lands before tensor memory is freed
-            tc_commit(sf_drain(which));
+            tc_commit(sf_drain(w_sf));
             for (uint32_t i = 0; i < GM_SPIN_LIMIT; ++i)
-                if (mbar_try_wait(sf_drain(which), 0u)) break;
+                if (mbar_try_wait(sf_drain(w_sf), 0u)) break;
         }
         __syncwarp();
     } else {
@@ -797,13 +810,13 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
     const int64_t grid = std::min<int64_t>(max_tiles, a.sms);
     if (grid <= 0) return cudaSuccess;
     if (swiglu)
-        k_gemm_fp4<BSQ_EPI_SWIGLU_BF16><<<(unsigned)grid, GM_THREADS, GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES, st>>>(
+        k_gemm_fp4<BSQ_EPI_SWIGLU_BF16><<<(unsigned)grid, GmCfg<BSQ_EPI_SWIGLU_BF16>::THREADS, GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES, st>>>(
             tmA, tmB, tmSFB, tmOut, p);
     else if (a.epilogue == BSQ_EPI_BF16)
-        k_gemm_fp4<BSQ_EPI_BF16><<<(unsigned)grid, GM_THREADS, GmCfg<BSQ_EPI_BF16>::SMEM_BYTES, st>>>(tmA, tmB, tmSFB,
+        k_gemm_fp4<BSQ_EPI_BF16><<<(unsigned)grid, GmCfg<BSQ_EPI_BF16>::THREADS, GmCfg<BSQ_EPI_BF16>::SMEM_BYTES, st>>>(tmA, tmB, tmSFB,
                                                                                                      tmOut, p);
     else
-        k_gemm_fp4<BSQ_EPI_F32><<<(unsigned)grid, GM_THREADS, GmCfg<BSQ_EPI_F32>::SMEM_BYTES, st>>>(tmA, tmB, tmSFB,
+        k_gemm_fp4<BSQ_EPI_F32><<<(unsigned)grid, GmCfg<BSQ_EPI_F32>::THREADS, GmCfg<BSQ_EPI_F32>::SMEM_BYTES, st>>>(tmA, tmB, tmSFB,
                                                                                                    tmOut, p);
     return cudaGetLastError();
 }
