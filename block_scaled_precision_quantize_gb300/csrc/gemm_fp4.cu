@@ -605,35 +605,32 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
             }
             tc_fence_after();
             if constexpr (EPI == BSQ_EPI_BF16) {
-                // Both 32-column halves come out of tensor memory before the
-                // accumulator is handed back (the first already packed to bf16,
-                // so at most 48 words are live); the staging and the stores,
-                // which may wait for the previous store to drain, come after.
+                // Both 32-column halves come out of tensor memory with one wait,
+                // and the accumulator is handed back before anything else; the
+                // packing, the staging and the stores (which may wait for the
+                // previous store to drain) come after.
                 const float s = s_early;
-                uint32_t pk[2][16];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t r[32];
-                    if (active) {
-                        tc_ld32_issue(tlane + 64 * part + 32 * h2, r);
-                        tc_ld_wait(r);
-                    }
-                    if (h2 == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[h2][j] = pack_bf16x2(__uint_as_float(r[2 * j]) * s, __uint_as_float(r[2 * j + 1]) * s);
+                uint32_t r[64];
+                if (active) {
+                    tc_ld32_issue(tlane + 64 * part, r);
+                    tc_ld32_issue(tlane + 64 * part + 32, r + 32);
+                    tc_ld_wait(r);
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
                 if (!active) continue;
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = pack_bf16x2(__uint_as_float(r[32 * h2 + 2 * j]) * s,
+                                            __uint_as_float(r[32 * h2 + 2 * j + 1]) * s);
                     stage_reuse(lane);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        stage_put(stage_buf, lane, c, pk[h2][4 * c], pk[h2][4 * c + 1], pk[h2][4 * c + 2], pk[h2][4 * c + 3]);
+                        stage_put(stage_buf, lane, c, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                     stage_store(stage_buf, lane, &tmOut, t.nt * 256 + 64 * part + 32 * h2, t.m0 + 32 * q);
                 }
                 continue;
