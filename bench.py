@@ -530,6 +530,20 @@ def quantizer_components(bsq, synth, dev, P):
 
     record("nvfp4_per_token_16384x2048", time_rotating(nv, n, 10 * n) * 1e3, b, n)
     del sets
+    # BF16 dequantization of NVFP4 (the dequantized backward's operands), 16384 x 2048, swizzled SF
+    b = 16384 * (1024 + 128 + 4) + 16384 * 2048 * 2
+    n = -(-l2_twice // b) + 1
+    c0, s0, t0 = bsq.quantize_nvfp4_per_token(xq, swizzled=True)
+    sets = [(c0.clone(), s0.clone(), t0.clone(), torch.empty(16384, 2048, dtype=torch.bfloat16, device=dev))
+            for _ in range(n)]
+
+    def dq(i):
+        c_, s_, t_, y_ = sets[i % n]
+        L.dequantize_nvfp4(c_.data_ptr(), s_.data_ptr(), t_.data_ptr(), 16384, 2048, 1, y_.data_ptr(), 2048,
+                           bsq.SF_SWIZZLED, None, st)
+
+    record("dequant_nvfp4_16384x2048", time_rotating(dq, n, 10 * n) * 1e3, b, n)
+    del sets
     # requant with Philox SR (and round-to-nearest), both targets, 16384 x 2048 and 16384 x 768
     for K in (2048, 768):
         b = (16384 * K // 2 + 16384 * K // 16 + 16384 * 4) + (K * 8192 + K * 1024 + K * 4) + (K * 16384 + K * 512)

@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "load", "build", "BsqError",
     "quantize_nvfp4_per_token", "quantize_nvfp4_per_expert", "quantize_mxfp8_rowcol",
-    "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
+    "dequantize_nvfp4", "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
     "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes",
     "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
@@ -57,6 +57,7 @@ _SIGS = {
     "quantize_nvfp4_per_token": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P, _P]),
     "quantize_nvfp4_per_expert": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P, _P]),
     "quantize_mxfp8_rowcol": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _U32, _P, _P]),
+    "dequantize_nvfp4": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _I64, _U32, _P, _P]),
     "bsq_requant_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "requant_transpose_sr": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _U64, _P, _SZ, _U32,
                                             _P, _P]),
@@ -191,6 +192,30 @@ def quantize_mxfp8_rowcol(x, row=True, col=True, swizzled=False, dev_status=None
                                         SF_SWIZZLED if swizzled else 0, _ptr(dev_status), _stream(dev)),
            "quantize_mxfp8_rowcol")
     return rc, rs, cc, cs
+
+
+def dequantize_nvfp4(codes, sf, scale, swizzled=False, y=None, dev_status=None):
+    """BF16 dequantization of NVFP4 codes [..., K/2] (the operands of the
+    dequantized backward).  `scale` holds one FP32 scale per row (per-token)
+    or per group of rows (per-expert weights [E, N, K/2] with scale [E]);
+    returns bf16 [..., K] (or writes `y`, rows of pitch y.stride(-2))."""
+    _cuda(codes, "codes")
+    _cuda(sf, "sf")
+    _cuda(scale, "scale")
+    K = 2 * codes.shape[-1]
+    rows = codes.numel() // codes.shape[-1] if codes.numel() else 0
+    groups = scale.numel()
+    if rows and (groups == 0 or rows % groups != 0):
+        raise BsqError(f"dequantize_nvfp4: {groups} scales for {rows} rows")
+    if y is None:
+        y = torch.empty(*codes.shape[:-1], K, dtype=torch.bfloat16, device=codes.device)
+    elif not (y.is_cuda and y.dtype == torch.bfloat16 and y.dim() == 2 and y.shape == (rows, K) and y.stride(-1) == 1):
+        raise BsqError("dequantize_nvfp4: y must be a CUDA bf16 [rows, K] tensor with unit column stride")
+    ldy = y.stride(-2) if y.dim() >= 2 else K
+    _check(load().dequantize_nvfp4(_ptr(codes), _ptr(sf), _ptr(scale), rows, K, rows // groups if rows else 1,
+                                   _ptr(y), ldy, SF_SWIZZLED if swizzled else 0, _ptr(dev_status),
+                                   _stream(codes.device)), "dequantize_nvfp4")
+    return y
 
 
 def requant_workspace_size(rows, K, nvfp4=True) -> int:

@@ -109,6 +109,25 @@ bsq_status quantize_nvfp4_per_token(const void* x, int64_t rows, int64_t K, int6
     return launched();
 }
 
+bsq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* sf, const float* scale, int64_t rows, int64_t K,
+                            int64_t group_rows, void* y, int64_t ldy, uint32_t flags, int32_t* dev_status,
+                            bsq_stream_t stream)
+{
+    (void)dev_status;
+    if (flags & ~BSQ_SF_SWIZZLED) return BSQ_ERR_FLAGS;
+    if (rows < 0 || K <= 0 || K % 16 != 0 || K > 65536 || ldy < K || group_rows <= 0 || rows > (int64_t)1 << 31)
+        return BSQ_ERR_SHAPE;
+    if (rows == 0) return BSQ_OK;
+    if (!codes || !sf || !scale || !y) return BSQ_ERR_NULL;
+    if (!a16(codes) || !a16(y) || ldy % 8 != 0 || (reinterpret_cast<uintptr_t>(sf) & 3u)) return BSQ_ERR_ALIGN;
+    int sms;
+    bsq_status st = current_device(&sms);
+    if (st != BSQ_OK) return st;
+    launch_dequant_nvfp4(codes, sf, scale, rows, K, group_rows, static_cast<uint16_t*>(y), ldy,
+                         (flags & BSQ_SF_SWIZZLED) != 0, sms, stream);
+    return launched();
+}
+
 bsq_status quantize_nvfp4_per_expert(const void* w, int64_t experts, int64_t rows, int64_t K, uint8_t* codes,
                                      uint8_t* sf, float* expert_scale, uint32_t flags, int32_t* dev_status,
                                      bsq_stream_t stream)

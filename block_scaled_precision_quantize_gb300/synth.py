@@ -19,6 +19,9 @@ Workloads (sizes as the MoE pages quote them):
             16384x768, to be NVFP4-quantized and then requantized
   deepseek  DeepSeek-V3-shaped expert layer: T=32768, H=7168, E=256, top-8,
             I=2048; router logits N(0,1) plus a Zipf(s=1.1) expert bias
+  nvfp4     random NVFP4 operands (codes, block scales, FP32 scales) for the
+            dequantization tests: uniform code bytes, block-scale bytes
+            uniform over the non-negative finite E4M3 codes, log-normal scales
 """
 from __future__ import annotations
 
@@ -144,3 +147,17 @@ WORKLOADS = {
     "requant": dict(shapes=[(16384, 2048), (16384, 768)], seed=7),
     "deepseek": dict(T=32768, H=7168, E=256, k=8, I=2048, seed=5, w_std=0.02, zipf_s=1.1),
 }
+
+
+def random_nvfp4(rows: int, K: int, seed: int, groups: int | None = None):
+    """Random NVFP4 operands: codes u8 [rows, K/2] (uniform bytes), block-scale
+    bytes u8 [rows, K/16] uniform over 0x00..0x7E (the non-negative finite
+    E4M3 codes, as the quantizers emit), and positive f32 scales, one per row
+    (or per group when `groups` is given), log-normal around 2^-8."""
+    g = rng(seed, 0)
+    codes = g.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+    sf = g.integers(0, 0x7F, size=(rows, K // 16), dtype=np.uint8)
+    n = rows if groups is None else groups
+    scale = np.exp2(g.normal(-8.0, 3.0, size=n)).astype(np.float32)
+    return codes, sf, scale
+

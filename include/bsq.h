@@ -127,6 +127,31 @@ bsq_status quantize_nvfp4_per_expert(const void* w, int64_t experts, int64_t row
                                      uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * dequantize_nvfp4: BF16 reconstruction of NVFP4 operands, for the
+ * dequantized backward mode ("LMSYS Drops Miles ...", "Recipe 2: Per-token
+ * NVFP4 for MoE experts"; "Miles Blackwell RL ...", "Un quantizzatore
+ * condiviso ...": the backward GEMMs run in BF16 on BF16 operands rebuilt
+ * from the exact low-precision values of the forward pass).  Per element
+ * y = bf16_rn(rn(rn(e2m1(code) * e4m3(sf)) * t)) in binary32, t the FP32
+ * scale of the element's row (activations, group_rows = 1) or of its group of
+ * group_rows consecutive rows (per-expert weights, group_rows = rows of one
+ * expert).  The inner product is exact; bf16_rn is round-to-nearest-even.
+ *   codes  [rows][K/2] (low nibble = even element), 16-byte aligned
+ *   sf     E4M3 block scales, linear [rows][K/16] or swizzled (BSQ_SF_SWIZZLED;
+ *          the buffer covers rows padded to 128), 4-byte aligned
+ *   scale  fp32 [rows] (group_rows = 1) or [ceil(rows / group_rows)]
+ *   y      out, bf16 [rows][ldy], K columns written; ldy >= K, ldy % 8 == 0,
+ *          16-byte aligned
+ * K % 16 == 0, 0 < K <= 65536; rows >= 0 (0 is a no-op).  E4M3 NaN codes
+ * are outside the contract.  All pointers are device pointers owned by the
+ * caller; the call only enqueues on `stream`.
+ * ------------------------------------------------------------------------- */
+bsq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* sf, const float* scale,
+                            int64_t rows, int64_t K, int64_t group_rows,
+                            void* y, int64_t ldy, uint32_t flags, int32_t* dev_status,
+                            bsq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * quantize_mxfp8_rowcol: MXFP8 row-wise and column-wise copies of one bf16
  * tensor in one pass, both from the original values ("LMSYS Drops Miles ...",
  * "Recipe 1: End-to-end MXFP8"; "Miles Blackwell RL ...", "Un quantizzatore

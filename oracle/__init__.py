@@ -217,6 +217,20 @@ def nvfp4_dequantize(codes, sf, t) -> np.ndarray:
     return out
 
 
+def nvfp4_dequantize_bf16(codes, sf, t_rows) -> np.ndarray:
+    """The BF16 operands of the dequantized backward mode ("LMSYS Drops Miles
+    ...", section "Recipe 2: Per-token NVFP4 for MoE experts": backward GEMMs
+    run in BF16 on BF16 dequantizations of the exact low-precision forward
+    operands).  The binary32 dequantization of the per-row recipe (element
+    value times its block scale, then times the row's FP32 scale, one
+    rounding per product), rounded to bf16 to nearest with ties to even.
+    READING: the pages fix no rounding for this step; BF16 round-to-nearest
+    of the binary32 value is the plainest.  t_rows: one scale per row (a
+    per-expert scale is repeated over its rows).  Returns uint16 bf16 bits."""
+    d = nvfp4_dequantize(codes, sf, t_rows)
+    return f64_to_bf16_array(d.astype(np.float64))
+
+
 def sf_swizzled_offset(row: int, kblock: int, K: int) -> int:
     return lib().bsqo_sf_swizzled_offset(int(row), int(kblock), int(K))
 

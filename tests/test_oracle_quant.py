@@ -347,3 +347,51 @@ def test_sr_draws_depend_only_on_output_index(O):
         assert np.array_equal(a[i], b[i])
     assert not np.array_equal(a[0], c[0])
     assert np.array_equal(a[1], c[1]) and np.array_equal(a[2], c[2])  # scales are RNE
+
+
+# ---------------------------------------------------------------- dequantize to bf16
+def _bf16_bits_of_exact(v):
+    """bf16 bits of a value that bf16 holds exactly (pure Python packing)."""
+    import struct
+    b = struct.unpack("<I", struct.pack("<f", v))[0]
+    assert b & 0xFFFF == 0, v
+    return b >> 16
+
+
+def test_dequant_bf16_exact_products(O):
+    # every code under block scales across the E4M3 range (0x01 = 2^-9 up to
+    # 0x7E = 448) and power-of-two row scales: each product has at most 5
+    # significant bits, so the bf16 result is the exact value; -0 keeps its sign
+    nib = np.arange(16, dtype=np.uint8)
+    packed = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    sfs = [0x01, 0x08, 0x30, 0x38, 0x3F, 0x7E]
+    codes = np.tile(packed, (len(sfs), 1))
+    sf = np.array(sfs, np.uint8).reshape(-1, 1)
+    for t in (1.0, 2.0 ** -7, 2.0 ** 20):
+        out = O.nvfp4_dequantize_bf16(codes, sf, np.full(len(sfs), t, np.float32))
+        for i, s in enumerate(sfs):
+            for k in range(16):
+                v = float(e2m1_val(k)) * float(e4m3_val(s)) * t
+                assert out[i, k] == _bf16_bits_of_exact(v), (hex(s), k, t)
+
+
+def test_dequant_bf16_rounding_against_numpy_and_torch(O):
+    # arbitrary row scales: binary32 products from numpy's float32 arithmetic,
+    # then torch's round-to-nearest-even conversion to bf16
+    codes, sf, t = synth.random_nvfp4(64, 256, seed=11)
+    out = O.nvfp4_dequantize_bf16(codes, sf, t)
+    v = e2m1_val(unpack(codes)).astype(np.float32)
+    s = np.repeat(e4m3_val(sf).astype(np.float32), 16, axis=1)
+    f32 = (v * s) * t[:, None]
+    ref = torch.from_numpy(np.ascontiguousarray(f32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(out, ref)
+
+
+def test_dequant_bf16_ties_to_even(O):
+    # 1.0 * (1 + 2^-8) is halfway between bf16 1.0 (0x3F80) and 1 + 2^-7
+    # (0x3F81): the even one, 0x3F80.  1 + 3 * 2^-8 is halfway between 0x3F81
+    # and 0x3F82: 0x3F82.
+    codes = np.full((1, 8), 0x22, np.uint8)  # code 2 (= 1.0) in both nibbles
+    sf = np.array([[0x38]], np.uint8)        # E4M3 1.0
+    assert (O.nvfp4_dequantize_bf16(codes, sf, np.array([1 + 2.0 ** -8], np.float32)) == 0x3F80).all()
+    assert (O.nvfp4_dequantize_bf16(codes, sf, np.array([1 + 3 * 2.0 ** -8], np.float32)) == 0x3F82).all()
