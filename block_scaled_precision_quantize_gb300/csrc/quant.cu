@@ -984,12 +984,14 @@ cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, cons
 // "Recipe 2: Per-token NVFP4 for MoE experts": the backward GEMMs run in BF16
 // on BF16 dequantizations of the exact low-precision forward operands).
 // y = bf16_rn(rn(rn(e2m1 * sf) * t)) with t the row's (per-token) or the
-// row's group's (per-expert) FP32 scale.  Bound by HBM: per element 0.5 B of
-// codes and 1/16 B of scale factor in, 2 B out.  Each thread takes BPT
-// consecutive 16-element blocks of one row: BPT = 4 when K % 64 == 0 (two
-// 16-byte code loads, the four SF bytes as one 4-byte word in either layout,
-// 128 bytes out), else one block (8 bytes of codes, one SF byte, 32 bytes
-// out); the grid strides over the rows' block groups.
+// row's group's (per-expert) FP32 scale.  Bound by HBM writes: per element
+// 0.5 B of codes and 1/16 B of scale factor in, 2 B out.  One warp per row;
+// lane l takes the row's 16-element blocks l, l + 32, l + 64, l + 96 (all
+// loads first, then the dequantization and the stores), so every store
+// instruction of the warp writes 1 KB of the row contiguously and every code
+// load reads 256 contiguous bytes.  Rows beyond the first wave of warps are
+// taken grid-stride.  (Four consecutive blocks per thread, 128-byte strided
+// stores, ran at 21.5 us on 16384 x 2048 against 17.1 us.)
 namespace {
 
 BSQ_DEVICE void store_bf16x16(uint16_t* dst, const uint32_t (&w)[8], bool vec32)
@@ -1011,46 +1013,44 @@ BSQ_DEVICE uint32_t bf16x2_rn(float lo, float hi)
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
-template <int BPT, bool SWZ>
+template <bool SWZ>
 __global__ void __launch_bounds__(256) k_dequant_nvfp4(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
                                                        const float* __restrict__ scale, int64_t rows, int K,
                                                        int64_t group_rows, uint16_t* __restrict__ y, int64_t ldy,
                                                        bool vec32)
 {
     const int kb = K >> 4;  // 16-element blocks per row
-    const int gpr = kb / BPT;
-    const int64_t total = rows * gpr;
+    const int lane = threadIdx.x & 31;
     const int64_t ncol_tiles = (kb + 3) >> 2;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = g / gpr;
-        const int c0 = (int)(g - row * gpr) * BPT;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nwarps) {
         const float t = __ldg(scale + (group_rows == 1 ? row : row / group_rows));
-        const uint8_t* src = codes + row * (int64_t)(K >> 1) + (int64_t)c0 * 8;
-        const int64_t sf_off = SWZ ? sf_swizzled(row, c0, ncol_tiles) : row * kb + c0;
-        uint32_t w[2 * BPT];
-        uint32_t sfw;
-        if constexpr (BPT == 4) {
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-            w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            sfw = __ldg(reinterpret_cast<const uint32_t*>(sf + sf_off));
-        } else {
-            const uint2 a = __ldg(reinterpret_cast<const uint2*>(src));
-            w[0] = a.x; w[1] = a.y;
-            sfw = __ldg(sf + sf_off);
-        }
-        uint16_t* dst = y + row * ldy + (int64_t)c0 * 16;
+        const uint8_t* crow = codes + row * (int64_t)(K >> 1);
+        uint16_t* yrow = y + row * ldy;
+        for (int j0 = 0; j0 < kb; j0 += 128) {
+            uint2 w[4];
+            uint32_t sb[4];
 #pragma unroll
-        for (int b = 0; b < BPT; ++b) {
-            const uint32_t sfb = (sfw >> (8 * b)) & 0xFFu;
-            float d[16];
-            e2m1x8_dequant(w[2 * b], sfb, t, *reinterpret_cast<float(*)[8]>(d));
-            e2m1x8_dequant(w[2 * b + 1], sfb, t, *reinterpret_cast<float(*)[8]>(d + 8));
-            uint32_t o[8];
+            for (int i = 0; i < 4; ++i) {
+                const int c = j0 + lane + 32 * i;
+                if (c < kb) {
+                    w[i] = __ldg(reinterpret_cast<const uint2*>(crow + (int64_t)c * 8));
+                    sb[i] = __ldg(sf + (SWZ ? sf_swizzled(row, c, ncol_tiles) : row * kb + c));
+                }
+            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = bf16x2_rn(d[2 * j], d[2 * j + 1]);
-            store_bf16x16(dst + 16 * b, o, vec32);
+            for (int i = 0; i < 4; ++i) {
+                const int c = j0 + lane + 32 * i;
+                if (c < kb) {
+                    float d[16];
+                    e2m1x8_dequant(w[i].x, sb[i], t, *reinterpret_cast<float(*)[8]>(d));
+                    e2m1x8_dequant(w[i].y, sb[i], t, *reinterpret_cast<float(*)[8]>(d + 8));
+                    uint32_t o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = bf16x2_rn(d[2 * j], d[2 * j + 1]);
+                    store_bf16x16(yrow + (int64_t)c * 16, o, vec32);
+                }
+            }
         }
     }
 }
@@ -1060,23 +1060,13 @@ __global__ void __launch_bounds__(256) k_dequant_nvfp4(const uint8_t* __restrict
 void launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* sf, const float* scale, int64_t rows, int64_t K,
                           int64_t group_rows, uint16_t* y, int64_t ldy, bool swz, int sms, cudaStream_t st)
 {
-    const int bpt = (K % 64 == 0) ? 4 : 1;
-    const int64_t total = rows * ((K / 16) / bpt);
-    const int64_t grid = std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
+    const int64_t grid = std::min<int64_t>((rows + 7) / 8, (int64_t)sms * 16);  // 8 warps (rows) per CTA
     if (grid <= 0) return;
     const bool vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) && (ldy % 16 == 0);
-    const int k = (int)K;
-    if (bpt == 4) {
-        if (swz)
-            k_dequant_nvfp4<4, true><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, k, group_rows, y, ldy, vec32);
-        else
-            k_dequant_nvfp4<4, false><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, k, group_rows, y, ldy, vec32);
-    } else {
-        if (swz)
-            k_dequant_nvfp4<1, true><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, k, group_rows, y, ldy, vec32);
-        else
-            k_dequant_nvfp4<1, false><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, k, group_rows, y, ldy, vec32);
-    }
+    if (swz)
+        k_dequant_nvfp4<true><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, (int)K, group_rows, y, ldy, vec32);
+    else
+        k_dequant_nvfp4<false><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, (int)K, group_rows, y, ldy, vec32);
 }
 
 }  // namespace bsq
