@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "load", "build", "BsqError",
     "quantize_nvfp4_per_token", "quantize_nvfp4_per_expert", "quantize_mxfp8_rowcol",
-    "dequantize_nvfp4", "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
+    "quantize_nvfp4_2d", "dequantize_nvfp4", "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
     "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes",
     "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
@@ -58,6 +58,7 @@ _SIGS = {
     "quantize_nvfp4_per_expert": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P, _P]),
     "quantize_mxfp8_rowcol": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _U32, _P, _P]),
     "dequantize_nvfp4": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _I64, _U32, _P, _P]),
+    "quantize_nvfp4_2d": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _U32, _P, _P]),
     "bsq_requant_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "requant_transpose_sr": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _U64, _P, _SZ, _U32,
                                             _P, _P]),
@@ -192,6 +193,25 @@ def quantize_mxfp8_rowcol(x, row=True, col=True, swizzled=False, dev_status=None
                                         SF_SWIZZLED if swizzled else 0, _ptr(dev_status), _stream(dev)),
            "quantize_mxfp8_rowcol")
     return rc, rs, cc, cs
+
+
+def quantize_nvfp4_2d(x, transposed=True, dev_status=None):
+    """2-D NVFP4 of bf16 x [rows, K] (rows % 16 == 0): one E4M3 scale per
+    16 x 16 tile and one FP32 scale per tensor.  Returns (codes [rows, K/2],
+    tile scales [rows/16, K/16], codes of x^T [K, rows/2], tile scales of x^T
+    [K/16, rows/16], tensor scale [1]); the transposed pair is None when
+    `transposed` is False."""
+    _cuda(x, "x")
+    rows, K = x.shape
+    dev = x.device
+    codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(rows // 16, K // 16, dtype=torch.uint8, device=dev)
+    codes_t = torch.empty(K, rows // 2, dtype=torch.uint8, device=dev) if transposed else None
+    sf_t = torch.empty(K // 16, rows // 16, dtype=torch.uint8, device=dev) if transposed else None
+    scale = torch.zeros(1, dtype=torch.float32, device=dev)
+    _check(load().quantize_nvfp4_2d(_ptr(x), rows, K, _ptr(codes), _ptr(sf), _ptr(codes_t), _ptr(sf_t), _ptr(scale),
+                                    0, _ptr(dev_status), _stream(dev)), "quantize_nvfp4_2d")
+    return codes, sf, codes_t, sf_t, scale
 
 
 def dequantize_nvfp4(codes, sf, scale, swizzled=False, y=None, dev_status=None):

@@ -109,6 +109,29 @@ bsq_status quantize_nvfp4_per_token(const void* x, int64_t rows, int64_t K, int6
     return launched();
 }
 
+bsq_status quantize_nvfp4_2d(const void* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf_tiles,
+                             uint8_t* codes_t, uint8_t* sf_tiles_t, float* tensor_scale, uint32_t flags,
+                             int32_t* dev_status, bsq_stream_t stream)
+{
+    (void)dev_status;
+    if (flags != 0) return BSQ_ERR_FLAGS;
+    if (rows < 0 || K <= 0 || K % 16 != 0 || K > 65536 || rows % 16 != 0 || rows > (int64_t)1 << 31)
+        return BSQ_ERR_SHAPE;
+    if (rows == 0) return BSQ_OK;
+    if (!x || !codes || !sf_tiles || !tensor_scale || (codes_t == nullptr) != (sf_tiles_t == nullptr))
+        return BSQ_ERR_NULL;
+    if (!a16(x) || !a16(codes) || (reinterpret_cast<uintptr_t>(codes_t) & 7u) ||
+        (reinterpret_cast<uintptr_t>(tensor_scale) & 3u))
+        return BSQ_ERR_ALIGN;
+    int sms;
+    bsq_status st = current_device(&sms);
+    if (st != BSQ_OK) return st;
+    if (launch_nvfp4_2d(static_cast<const uint16_t*>(x), rows, K, codes, sf_tiles, codes_t, sf_tiles_t, tensor_scale,
+                        sms, stream) != cudaSuccess)
+        return BSQ_ERR_CUDA;
+    return launched();
+}
+
 bsq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* sf, const float* scale, int64_t rows, int64_t K,
                             int64_t group_rows, void* y, int64_t ldy, uint32_t flags, int32_t* dev_status,
                             bsq_stream_t stream)

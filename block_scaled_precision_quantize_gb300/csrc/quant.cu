@@ -979,6 +979,172 @@ cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, cons
     return requant_passes(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, sr, swz, st);
 }
 
+// ---------------------------------------------------------------- 2-D NVFP4
+// One E4M3 scale per 16 x 16 tile and one FP32 scale per tensor ("End-to-End
+// 4-Bit Training", section "第二个决定": square block scales are the same
+// before and after the transpose, so the transposed backward operand is the
+// same codes and scales rearranged, with no requantization; the price is 256
+// values under one scale).
+// Pass 1, the tensor maximum: grid-stride 16-byte loads, folded per warp and
+// per CTA, one atomic per CTA.
+// Pass 2: a CTA takes 128 rows x 128 columns; warp w the 16-row strip w of
+// it.  Lanes 4p .. 4p + 3 take 4 columns each of tile p over its 16 rows
+// (8-byte loads: every load instruction reads 256 contiguous bytes of a row,
+// and 32 registers hold the data); the tile maximum is folded over the four
+// lanes.  The row-major codes leave as 2 bytes per lane and row (64
+// contiguous bytes per instruction).  The transposed codes (8 bytes = 16 rows
+// per column and strip) meet in shared memory, in 72-byte rows with the strip
+// slot rotated by column so that a warp's 256 bytes take the minimum two
+// wavefronts; two threads then write each column's 64 bytes (the CTA's 128
+// rows) of the transposed operand, 32 bytes each.
+namespace {
+
+__global__ void __launch_bounds__(256) k_tensor_amax(const uint16_t* __restrict__ x, int64_t n8,
+                                                     unsigned int* __restrict__ amax_bits)
+{
+    __shared__ uint32_t s_m[8];
+    uint32_t m = 0;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 7 * stride < n8; i += 8 * stride) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = ldg_stream(x + 8 * (i + u * stride));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            uint32_t a = absmax_bf16x2(0u, v[u].x);
+            a = absmax_bf16x2(a, v[u].y);
+            a = absmax_bf16x2(a, v[u].z);
+            a = absmax_bf16x2(a, v[u].w);
+            m = max(m, fold_halves(a));
+        }
+    }
+    for (; i < n8; i += stride) {
+        const uint4 v = ldg_stream(x + 8 * i);
+        uint32_t a = absmax_bf16x2(0u, v.x);
+        a = absmax_bf16x2(a, v.y);
+        a = absmax_bf16x2(a, v.z);
+        a = absmax_bf16x2(a, v.w);
+        m = max(m, fold_halves(a));
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_m[w]);
+        if (m) atomicMax(amax_bits, m << 16);
+    }
+}
+
+template <bool T_OUT>
+__global__ void __launch_bounds__(256) k_nvfp4_2d(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                  const float* __restrict__ tscale, uint8_t* __restrict__ codes,
+                                                  uint8_t* __restrict__ sf, uint8_t* __restrict__ codes_t,
+                                                  uint8_t* __restrict__ sf_t, bool vec32_t)
+{
+    __shared__ uint2 s_t[128][9];   // [column of the CTA tile][rotated strip slot], one slot of padding
+    __shared__ uint8_t s_sf[8][8];  // [column tile][row strip]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ctiles = (K + 127) >> 7;
+    const int64_t nblk = ((rows + 127) >> 7) * ctiles;
+    const float t = __ldg(tscale);
+    const float six_t = __fmul_rn(6.0f, t);
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t R0 = (blk / ctiles) << 7, C0 = (blk % ctiles) << 7;
+        const int64_t r0 = R0 + 16 * warp, c0 = C0 + 4 * lane;  // this lane's first row and column
+        const bool valid = r0 < rows && c0 < K;                  // K % 16 == 0: the lanes of a tile agree
+        uint2 v[16];
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = valid ? __ldcs(reinterpret_cast<const uint2*>(x + (r0 + i) * K + c0)) : make_uint2(0u, 0u);
+            m = max(m, fold_halves(absmax_bf16x2(absmax_bf16x2(0u, v[i].x), v[i].y)));
+        }
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        uint32_t sfb = 0u;
+        float enc = 0.0f;
+        if (t != 0.0f) {
+            const BlockScale bs = nvfp4_block_scale(bf16mag_to_f32(m), six_t, t);
+            sfb = bs.sf;
+            enc = bs.enc;
+        }
+        uint32_t w[16];  // 4 codes (16 bits) of row i
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            w[i] = (t != 0.0f) ? (e2m1x8(__fmul_rn(bf16_lo(v[i].x), enc), __fmul_rn(bf16_hi(v[i].x), enc),
+                                         __fmul_rn(bf16_lo(v[i].y), enc), __fmul_rn(bf16_hi(v[i].y), enc), 0.0f, 0.0f,
+                                         0.0f, 0.0f) & 0xFFFFu)
+                               : 0u;
+            if (valid) *reinterpret_cast<uint16_t*>(codes + (r0 + i) * (K >> 1) + (c0 >> 1)) = (uint16_t)w[i];
+        }
+        if (valid && (lane & 3) == 0) sf[(r0 >> 4) * (K >> 4) + (c0 >> 4)] = (uint8_t)sfb;
+        if constexpr (T_OUT) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    lo |= ((w[i] >> (4 * j)) & 0xFu) << (4 * i);
+                    hi |= ((w[i + 8] >> (4 * j)) & 0xFu) << (4 * i);
+                }
+                const int col = 4 * lane + j;
+                s_t[col][(warp + (col >> 4)) & 7] = make_uint2(lo, hi);
+            }
+            if ((lane & 3) == 0) s_sf[lane >> 2][warp] = (uint8_t)sfb;
+            __syncthreads();
+            // column C0 + c of x = row C0 + c of the transposed operand; thread 2c + h writes
+            // its row strips 4h .. 4h + 3 (32 bytes)
+            const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
+            const int64_t col = C0 + c;
+            const int nst = (int)(((rows - R0) >> 4) < 8 ? ((rows - R0) >> 4) : 8);  // row strips present
+            if (col < K) {
+                uint2 q[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[k] = s_t[c][(4 * h + k + (c >> 4)) & 7];
+                uint2* dst = reinterpret_cast<uint2*>(codes_t + col * (rows >> 1) + (R0 >> 1)) + 4 * h;
+                if (nst == 8 && vec32_t) {
+                    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(q[0].x),
+                                 "r"(q[0].y), "r"(q[1].x), "r"(q[1].y), "r"(q[2].x), "r"(q[2].y), "r"(q[3].x),
+                                 "r"(q[3].y)
+                                 : "memory");
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (4 * h + k < nst) dst[k] = q[k];
+                }
+            }
+            if (threadIdx.x < 64) {
+                const int ct = threadIdx.x >> 3, k = threadIdx.x & 7;
+                if (k < nst && C0 + 16 * ct < K) sf_t[((C0 >> 4) + ct) * (rows >> 4) + (R0 >> 4) + k] = s_sf[ct][k];
+            }
+            __syncthreads();
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf,
+                            uint8_t* codes_t, uint8_t* sf_t, float* tscale, int sms, cudaStream_t st)
+{
+    cudaError_t err = cudaMemsetAsync(tscale, 0, sizeof(float), st);
+    if (err != cudaSuccess) return err;
+    const int64_t n8 = rows * K / 8;
+    k_tensor_amax<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)sms * 8)), 256, 0,
+                    st>>>(x, n8, reinterpret_cast<unsigned int*>(tscale));
+    launch_group_finalize(tscale, 1, st);
+    const int64_t nblk = ((rows + 127) >> 7) * ((K + 127) >> 7);
+    const int64_t grid = std::min<int64_t>(nblk, (int64_t)sms * 8);
+    if (grid <= 0) return cudaSuccess;
+    const bool vec32_t = codes_t && (reinterpret_cast<uintptr_t>(codes_t) % 32 == 0) && ((rows >> 1) % 32 == 0);
+    if (codes_t)
+        k_nvfp4_2d<true><<<(unsigned)grid, 256, 0, st>>>(x, rows, K, tscale, codes, sf, codes_t, sf_t, vec32_t);
+    else
+        k_nvfp4_2d<false><<<(unsigned)grid, 256, 0, st>>>(x, rows, K, tscale, codes, sf, nullptr, nullptr, false);
+    return cudaSuccess;
+}
+
 // ---------------------------------------------------------------- dequantize
 // BF16 operands for the dequantized backward mode ("LMSYS Drops Miles ...",
 // "Recipe 2: Per-token NVFP4 for MoE experts": the backward GEMMs run in BF16

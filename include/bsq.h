@@ -127,6 +127,31 @@ bsq_status quantize_nvfp4_per_expert(const void* w, int64_t experts, int64_t row
                                      uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * quantize_nvfp4_2d: NVFP4 with one E4M3 scale per 16 x 16 square block and
+ * one FP32 scale per tensor, emitting the row-major operand and, optionally,
+ * the transposed one ("End-to-End 4-Bit Training", "第二个决定": square block
+ * scales are the same before and after the transpose, so the backward
+ * operand needs no requantization; the page's authors found 256 values per
+ * scale too coarse next to outliers and requantized instead).
+ * t = amax(|x|) / 2688 over the whole tensor; per tile, the per-row recipe's
+ * block steps with the tile's maximum: s = E4M3(amax_tile / (6 t)),
+ * d = s * t, code = E2M1(x * (1 / d)).  t == 0 gives all-zero codes and scales.
+ *   x            bf16 [rows][K], contiguous, 16-byte aligned
+ *   codes        out, [rows][K/2] (low nibble = even column), 16-byte aligned
+ *   sf_tiles     out, E4M3 [rows/16][K/16] (linear)
+ *   codes_t      out, [K][rows/2]: the codes of x^T, 8-byte aligned (NULL:
+ *                skip, with sf_tiles_t)
+ *   sf_tiles_t   out, E4M3 [K/16][rows/16] (= sf_tiles transposed)
+ *   tensor_scale out, fp32 [1]
+ * rows % 16 == 0, K % 16 == 0, 0 < K <= 65536; rows == 0 is a no-op.
+ * flags must be 0.  The result equals quantizing x^T with the same recipe.
+ * ------------------------------------------------------------------------- */
+bsq_status quantize_nvfp4_2d(const void* x, int64_t rows, int64_t K,
+                             uint8_t* codes, uint8_t* sf_tiles,
+                             uint8_t* codes_t, uint8_t* sf_tiles_t, float* tensor_scale,
+                             uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * dequantize_nvfp4: BF16 reconstruction of NVFP4 operands, for the
  * dequantized backward mode ("LMSYS Drops Miles ...", "Recipe 2: Per-token
  * NVFP4 for MoE experts"; "Miles Blackwell RL ...", "Un quantizzatore

@@ -77,6 +77,7 @@ def _declare(L):
         "bsqo_nvfp4_quantize_rows_given_t": (None, [_P, _I64, _I64, _P, _INT, _P, _P]),
         "bsqo_nvfp4_quantize_group": (None, [_P, _I64, _I64, _I64, _P, _P, _P]),
         "bsqo_nvfp4_dequantize": (None, [_P, _P, _P, _I64, _I64, _P]),
+        "bsqo_nvfp4_quantize_2d": (None, [_P, _I64, _I64, _P, _P, _P]),
         "bsqo_nvfp4_block_candidate": (None, [_P, ctypes.c_float, ctypes.c_float, _P, _P, _P]),
         "bsqo_sf_swizzled_offset": (_I64, [_I64, _I64, _I64]),
         "bsqo_sf_swizzle": (None, [_P, _I64, _I64, _P]),
@@ -215,6 +216,20 @@ def nvfp4_dequantize(codes, sf, t) -> np.ndarray:
     out = np.empty((rows, K), np.float32)
     lib().bsqo_nvfp4_dequantize(_ptr(codes), _ptr(sf), _ptr(t), rows, K, _ptr(out))
     return out
+
+
+def nvfp4_quantize_2d(x_bits: np.ndarray):
+    """2-D NVFP4 of bf16 x [rows, K]: one E4M3 scale per 16 x 16 tile and one
+    FP32 scale per tensor ("End-to-End 4-Bit Training", section "第二个决定": square
+    block scales are the same before and after the transpose).  Returns
+    (codes [rows, K/2], tile scales [rows/16, K/16], t)."""
+    x = _c(x_bits, np.uint16)
+    rows, K = x.shape
+    codes = np.empty((rows, K // 2), np.uint8)
+    sf = np.empty((rows // 16, K // 16), np.uint8)
+    t = np.empty(1, np.float32)
+    lib().bsqo_nvfp4_quantize_2d(_ptr(x), rows, K, _ptr(codes), _ptr(sf), _ptr(t))
+    return codes, sf, float(t[0])
 
 
 def nvfp4_dequantize_bf16(codes, sf, t_rows) -> np.ndarray:

@@ -356,6 +356,56 @@ EXPORT void bsqo_nvfp4_quantize_group(const uint16_t* x, int64_t groups, int64_t
     free(xf);
 }
 
+/* ------------------------------------------------------------------------
+ * 2-D NVFP4: one E4M3 scale per 16 x 16 square block.  [TML-ZH] "第二个决定":
+ * the alternative NVIDIA offers to requantizing in the backward pass is
+ * square 16 x 16 block scaling, whose scale factors are the same before and
+ * after the transpose; with 256 values under one scale a single large value
+ * pushes the other 255 to zero, which is why the page's authors took the
+ * dequantize-transpose-requantize route instead.
+ * READING: the outer FP32 scale must not change under the transpose either,
+ * so it is one per tensor, t = rn(amax / 2688) over the whole tensor (as for
+ * weights); each tile then follows steps 3-4 of the per-row recipe with the
+ * tile's amax in place of the 16-block's.  If t == 0 every code and scale is
+ * 0.  Outputs: codes [rows][K/2] (the row-major packing of the 1 x 16
+ * layout, low nibble = even column) and tile scales [rows/16][K/16].
+ * rows % 16 == 0, K % 16 == 0.
+ * ---------------------------------------------------------------------- */
+EXPORT void bsqo_nvfp4_quantize_2d(const uint16_t* x, int64_t rows, int64_t K,
+                                   uint8_t* codes, uint8_t* sf_tiles, float* t_out)
+{
+    if (rows <= 0 || K <= 0) {
+        *t_out = 0.0f;
+        return;
+    }
+    float amax = 0.0f;
+    for (int64_t i = 0; i < rows * K; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(x[i])));
+    const float t = nvfp4_scale_from_amax(amax);
+    *t_out = t;
+    memset(codes, 0, (size_t)(rows * K / 2));
+    memset(sf_tiles, 0, (size_t)((rows / 16) * (K / 16)));
+    if (t == 0.0f) return;
+    for (int64_t tr = 0; tr < rows / 16; ++tr)
+        for (int64_t tc = 0; tc < K / 16; ++tc) {
+            float amax_t = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j)
+                    amax_t = fmaxf(amax_t, fabsf(bf16_to_f32(x[(16 * tr + i) * K + 16 * tc + j])));
+            const float denom = 6.0f * t;
+            const uint32_t sf = bsqo_e4m3_encode(amax_t / denom);
+            const float d = bsqo_e4m3_decode(sf) * t;
+            float enc = (d == 0.0f) ? 0.0f : 1.0f / d;
+            if (isinf(enc)) enc = FLT_MAX;
+            sf_tiles[tr * (K / 16) + tc] = (uint8_t)sf;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    const int64_t r = 16 * tr + i, k = 16 * tc + j;
+                    const uint32_t code = bsqo_e2m1_encode(bf16_to_f32(x[r * K + k]) * enc);
+                    codes[r * (K / 2) + k / 2] |= (uint8_t)((k & 1) ? (code << 4) : code);
+                }
+        }
+}
+
 /* Step 5 above: binary32 dequantization of an NVFP4 tensor (per-row t). */
 EXPORT void bsqo_nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* t,
                                   int64_t rows, int64_t K, float* out)

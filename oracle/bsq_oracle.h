@@ -61,6 +61,10 @@ void bsqo_mxfp8_quantize_rowcol(const uint16_t* x, int64_t rows, int64_t K, int6
                                 uint8_t* row_codes, uint8_t* row_sf,
                                 uint8_t* col_codes, uint8_t* col_sf);
 
+/* 2-D NVFP4: one E4M3 scale per 16 x 16 tile, one FP32 scale per tensor */
+void bsqo_nvfp4_quantize_2d(const uint16_t* x, int64_t rows, int64_t K,
+                            uint8_t* codes, uint8_t* sf_tiles, float* t_out);
+
 /* backward dequantize -> transpose -> requantize */
 void bsqo_requant_transpose(const uint8_t* codes, const uint8_t* sf, const float* t,
                             int64_t rows, int64_t K, int sr, uint64_t seed,

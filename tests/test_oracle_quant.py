@@ -395,3 +395,63 @@ def test_dequant_bf16_ties_to_even(O):
     sf = np.array([[0x38]], np.uint8)        # E4M3 1.0
     assert (O.nvfp4_dequantize_bf16(codes, sf, np.array([1 + 2.0 ** -8], np.float32)) == 0x3F80).all()
     assert (O.nvfp4_dequantize_bf16(codes, sf, np.array([1 + 3 * 2.0 ** -8], np.float32)) == 0x3F82).all()
+
+
+# ---------------------------------------------------------------- 2-D (16 x 16) block scales
+def _transpose_codes(codes):
+    """Packed [rows, K/2] -> the packed codes of the transpose, [K, rows/2]."""
+    u = unpack(codes).T
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_2d_transpose_invariance(O):
+    # the tile maxima and the per-tensor scale do not change under the
+    # transpose and the element rule is elementwise, so quantizing x^T gives
+    # the transposed codes and tile scales
+    x = synth.normal_with_outliers(64, 96, seed=21)
+    c, s, t = O.nvfp4_quantize_2d(x)
+    cT, sT, tT = O.nvfp4_quantize_2d(np.ascontiguousarray(x.T))
+    assert t == tT
+    np.testing.assert_array_equal(cT, _transpose_codes(c))
+    np.testing.assert_array_equal(sT, s.T)
+
+
+def test_2d_uniform_tile_closed_form(O):
+    # x = 1 everywhere: t = 1/2688, tile scale E4M3(1 / (6 t)) = 448 (0x7E),
+    # d = 448 t = 1/6, so every element becomes 6 (code 7)
+    x = np.full((16, 32), 0x3F80, np.uint16)
+    c, s, t = O.nvfp4_quantize_2d(x)
+    assert np.float32(t) == np.float32(1.0) / np.float32(2688.0)
+    assert (s == 0x7E).all()
+    assert (unpack(c) == 7).all()
+
+
+def test_2d_reduces_to_per_row_for_repeated_rows(O):
+    # identical rows: each tile's maximum is its 16-blocks' maximum and the
+    # per-tensor scale is every row's scale, so the result is the 1 x 16 one
+    row = synth.normal_with_outliers(1, 64, seed=22)
+    x = np.repeat(row, 32, axis=0)
+    c2, s2, t2 = O.nvfp4_quantize_2d(x)
+    c1, s1, t1 = O.nvfp4_quantize_rows(x)
+    assert (np.asarray(t1, np.float32) == np.float32(t2)).all()
+    np.testing.assert_array_equal(c2, c1)
+    np.testing.assert_array_equal(np.repeat(s2, 16, axis=0), s1)
+
+
+def test_2d_one_outlier_flushes_its_tile(O):
+    # the page's objection to square blocks: one large value among 256 pushes
+    # the other 255 to zero, while with 1 x 16 blocks only the outlier's own
+    # block loses its small values
+    x = np.full((16, 16), 0x3F80, np.uint16)  # 1.0
+    x[5, 9] = 0x447A                          # 1000.0
+    u2 = unpack(O.nvfp4_quantize_2d(x)[0])
+    assert u2[5, 9] == 7
+    assert (np.delete(u2.ravel(), 5 * 16 + 9) == 0).all()
+    u1 = unpack(O.nvfp4_quantize_rows(x)[0])
+    assert (u1[np.arange(16) != 5] == 7).all()
+    assert u1[5, 9] == 7 and (np.delete(u1[5], 9) == 0).all()
+
+
+def test_2d_zero_tensor(O):
+    c, s, t = O.nvfp4_quantize_2d(np.zeros((32, 48), np.uint16))
+    assert t == 0.0 and not c.any() and not s.any()
