@@ -105,7 +105,7 @@ bsq_status quantize_nvfp4_per_token(const void* x, int64_t rows, int64_t K, int6
     bsq_status st = current_device(&sms);
     if (st != BSQ_OK) return st;
     launch_nvfp4_rows(static_cast<const uint16_t*>(x), rows, K, ldx, codes, sf, row_scale, nullptr, 1,
-                      (flags & BSQ_FOUR_SIX) != 0, (flags & BSQ_SF_SWIZZLED) != 0, sms, stream);
+                      (flags & BSQ_FOUR_SIX) != 0, (flags & BSQ_SF_SWIZZLED) != 0, sms, true, stream);
     return launched();
 }
 
@@ -170,7 +170,7 @@ bsq_status quantize_nvfp4_per_expert(const void* w, int64_t experts, int64_t row
     if (cudaMemsetAsync(expert_scale, 0, (size_t)experts * sizeof(float), stream) != cudaSuccess) return BSQ_ERR_CUDA;
     launch_group_amax(x, experts * rows, K, rows, expert_scale, sms, stream);
     launch_nvfp4_rows(x, experts * rows, K, K, codes, sf, nullptr, expert_scale, rows, false,
-                      (flags & BSQ_SF_SWIZZLED) != 0, sms, stream);
+                      (flags & BSQ_SF_SWIZZLED) != 0, sms, false, stream);
     launch_group_finalize(expert_scale, experts, stream);
     return launched();
 }
@@ -416,7 +416,7 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
     stage_mark(3, stream);
 
     launch_nvfp4_rows(reinterpret_cast<const uint16_t*>(ws + L.h), cap, I, I, ws + L.hq_codes, ws + L.hq_sf,
-                      F32(L.hq_scale), nullptr, 1, f46, true, sms, stream);
+                      F32(L.hq_scale), nullptr, 1, f46, true, sms, false, stream);
     stage_mark(4, stream);
 
     GemmArgs g2 = g1;

@@ -28,6 +28,16 @@ constexpr float kNvfp4ScaleDivisor = 2688.0f;  // 6 (E2M1 max) * 448 (E4M3 max)
 constexpr float kFltMax = 3.402823466e+38f;
 
 // ---------------------------------------------------------------- status
+// Programmatic dependent launch: wait until the grid this one depends on has
+// completed (its writes visible), then let the next grid in the stream start
+// its launch.  Both are no-ops when the kernel was launched without the
+// programmatic-serialization attribute.
+BSQ_DEVICE void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 BSQ_DEVICE void report(int32_t* dev_status, int32_t code)
 {
     if (dev_status != nullptr) atomicCAS(dev_status, BSQ_DEV_OK, code);

@@ -8,7 +8,7 @@ namespace bsq {
 
 void launch_nvfp4_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* sf,
                        float* row_scale, const float* group_amax, int64_t rows_per_group, bool four_six, bool swz,
-                       int sms, cudaStream_t st);
+                       int sms, bool pdl, cudaStream_t st);
 void launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t rows_per_group, float* group_amax,
                        int sms, cudaStream_t st);
 void launch_group_finalize(float* scale, int64_t groups, cudaStream_t st);

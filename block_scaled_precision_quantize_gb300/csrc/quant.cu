@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__
                                                     uint8_t* __restrict__ sf, float* __restrict__ row_scale,
                                                     const float* __restrict__ group_amax, int64_t rpg)
 {
+    pdl_enter();
     constexpr int RPW = 32 / LPR;  // rows per warp step
     const int lane = threadIdx.x & 31, lr = lane % LPR;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows_wide(const uint16_t* __restr
                                                          uint8_t* __restrict__ sf, float* __restrict__ row_scale,
                                                          const float* __restrict__ group_amax, int64_t rpg)
 {
+    pdl_enter();
     constexpr int WPR = 4, BPL = 4;
     __shared__ uint32_t part_max[8];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows_long(const uint16_t* __restr
                                                          uint8_t* __restrict__ sf, float* __restrict__ row_scale,
                                                          const float* __restrict__ group_amax, int64_t rpg)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int nblk = (int)(K >> 4);
@@ -326,6 +329,7 @@ __global__ void __launch_bounds__(512) k_mxfp8_rowcol(const uint16_t* __restrict
                                                       uint8_t* __restrict__ row_sf, uint8_t* __restrict__ col_codes,
                                                       uint8_t* __restrict__ col_sf)
 {
+    pdl_enter();
     __shared__ __align__(16) uint4 tile[MX_TILE * 16];
     __shared__ uint8_t sfrow[MX_TILE][4];  // row scale bytes of the tile's 4 blocks per row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -784,6 +788,32 @@ __global__ void k_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, i
 
 // ---------------------------------------------------------------------------
 // Launchers.
+// A launch with programmatic dependent launch allowed (pdl): the grid may be
+// launched while the previous one in the stream drains, and its kernel waits
+// for it in pdl_enter() before touching memory.  The standalone quantizer
+// entry points use it, so back-to-back calls overlap one call's tail with the
+// next one's launch; the MoE forward launches plainly (there the GEMM's
+// CTAs need the SMs to themselves).
+template <typename... KArgs, typename... Args>
+static void launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, bool pdl, cudaStream_t st, Args... args)
+{
+    if (!pdl) {
+        kernel<<<grid, block, 0, st>>>(args...);
+        return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 static int grid_for(int64_t warps_needed, int sms)
 {
     const int64_t blocks = (warps_needed + 7) / 8;
@@ -793,33 +823,35 @@ static int grid_for(int64_t warps_needed, int sms)
 
 template <bool F46, bool SWZ, int TM>
 static void launch_rows_t(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* sf,
-                          float* rs, const float* gam, int64_t rpg, int sms, cudaStream_t st)
+                          float* rs, const float* gam, int64_t rpg, int sms, bool pdl, cudaStream_t st)
 {
     const int nblk = (int)(K >> 4);
     const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
     const int grid = grid_for(rows_iter, sms);
     if (nblk == 48)  // e.g. K = 768: a half-warp per row, 3 blocks per lane
-        k_nvfp4_rows<3, F46, SWZ, TM, 16><<<grid_for((rows_iter + 1) / 2, sms), 256, 0, st>>>(x, rows, K, ldx, codes, sf,
-                                                                                               rs, gam, rpg);
+        launch_k(k_nvfp4_rows<3, F46, SWZ, TM, 16>, dim3(grid_for((rows_iter + 1) / 2, sms)), dim3(256), pdl, st, x,
+                 rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 32)
-        k_nvfp4_rows<1, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
+        launch_k(k_nvfp4_rows<1, F46, SWZ, TM>, dim3(grid), dim3(256), pdl, st, x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 64)
-        k_nvfp4_rows<2, F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
+        launch_k(k_nvfp4_rows<2, F46, SWZ, TM>, dim3(grid), dim3(256), pdl, st, x, rows, K, ldx, codes, sf, rs, gam, rpg);
     else if (nblk <= 128)  // ~70 registers a thread: CTAs of 4 warps fill an SM (28 warps) better than of 8 (24)
-        k_nvfp4_rows<4, F46, SWZ, TM><<<2 * grid, 128, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
+        launch_k(k_nvfp4_rows<4, F46, SWZ, TM>, dim3(2 * grid), dim3(128), pdl, st, x, rows, K, ldx, codes, sf, rs, gam,
+                 rpg);
     else if (nblk <= 512)
-        k_nvfp4_rows_wide<F46, SWZ, TM><<<grid_for(rows_iter * 4, sms), 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs,
-                                                                                     gam, rpg);
+        launch_k(k_nvfp4_rows_wide<F46, SWZ, TM>, dim3(grid_for(rows_iter * 4, sms)), dim3(256), pdl, st, x, rows, K,
+                 ldx, codes, sf, rs, gam, rpg);
     else
-        k_nvfp4_rows_long<F46, SWZ, TM><<<grid, 256, 0, st>>>(x, rows, K, ldx, codes, sf, rs, gam, rpg);
+        launch_k(k_nvfp4_rows_long<F46, SWZ, TM>, dim3(grid), dim3(256), pdl, st, x, rows, K, ldx, codes, sf, rs, gam,
+                 rpg);
 }
 
 void launch_nvfp4_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* sf,
                        float* row_scale, const float* group_amax, int64_t rpg, bool four_six, bool swz, int sms,
-                       cudaStream_t st)
+                       bool pdl, cudaStream_t st)
 {
     const bool per_group = group_amax != nullptr;
-#define BSQ_ROWS(F, S, T) launch_rows_t<F, S, T>(x, rows, K, ldx, codes, sf, row_scale, group_amax, rpg, sms, st)
+#define BSQ_ROWS(F, S, T) launch_rows_t<F, S, T>(x, rows, K, ldx, codes, sf, row_scale, group_amax, rpg, sms, pdl, st)
     if (per_group) {
         if (swz) BSQ_ROWS(false, true, 1); else BSQ_ROWS(false, false, 1);
     } else if (four_six) {
@@ -846,7 +878,7 @@ void launch_mxfp8_rowcol(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx
 {
     dim3 grid((unsigned)((K + MX_TILE - 1) / MX_TILE), (unsigned)((rows + MX_TILE - 1) / MX_TILE));
     const bool row = rc != nullptr, col = cc != nullptr;
-#define BSQ_MX(S, R, C) k_mxfp8_rowcol<S, R, C><<<grid, 512, 0, st>>>(x, rows, K, ldx, rc, rs, cc, cs)
+#define BSQ_MX(S, R, C) launch_k(k_mxfp8_rowcol<S, R, C>, grid, dim3(512), true, st, x, rows, K, ldx, rc, rs, cc, cs)
     if (swz) {
         if (row && col) BSQ_MX(true, true, true); else if (row) BSQ_MX(true, true, false); else BSQ_MX(true, false, true);
     } else {
@@ -1042,6 +1074,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_2d(const uint16_t* __restrict__ x
                                                   uint8_t* __restrict__ sf, uint8_t* __restrict__ codes_t,
                                                   uint8_t* __restrict__ sf_t, bool vec32_t)
 {
+    pdl_enter();
     __shared__ uint2 s_t[128][9];   // [column of the CTA tile][rotated strip slot], one slot of padding
     __shared__ uint8_t s_sf[8][8];  // [column tile][row strip]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1139,9 +1172,11 @@ cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t rows, int64_t K, uint8_t*
     if (grid <= 0) return cudaSuccess;
     const bool vec32_t = codes_t && (reinterpret_cast<uintptr_t>(codes_t) % 32 == 0) && ((rows >> 1) % 32 == 0);
     if (codes_t)
-        k_nvfp4_2d<true><<<(unsigned)grid, 256, 0, st>>>(x, rows, K, tscale, codes, sf, codes_t, sf_t, vec32_t);
+        launch_k(k_nvfp4_2d<true>, dim3((unsigned)grid), dim3(256), true, st, x, rows, K, (const float*)tscale, codes,
+                 sf, codes_t, sf_t, vec32_t);
     else
-        k_nvfp4_2d<false><<<(unsigned)grid, 256, 0, st>>>(x, rows, K, tscale, codes, sf, nullptr, nullptr, false);
+        launch_k(k_nvfp4_2d<false>, dim3((unsigned)grid), dim3(256), true, st, x, rows, K, (const float*)tscale, codes,
+                 sf, (uint8_t*)nullptr, (uint8_t*)nullptr, false);
     return cudaSuccess;
 }
 
@@ -1185,6 +1220,7 @@ __global__ void __launch_bounds__(256) k_dequant_nvfp4(const uint8_t* __restrict
                                                        int64_t group_rows, uint16_t* __restrict__ y, int64_t ldy,
                                                        bool vec32)
 {
+    pdl_enter();
     const int kb = K >> 4;  // 16-element blocks per row
     const int lane = threadIdx.x & 31;
     const int64_t ncol_tiles = (kb + 3) >> 2;
@@ -1230,9 +1266,11 @@ void launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* sf, const float* 
     if (grid <= 0) return;
     const bool vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) && (ldy % 16 == 0);
     if (swz)
-        k_dequant_nvfp4<true><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, (int)K, group_rows, y, ldy, vec32);
+        launch_k(k_dequant_nvfp4<true>, dim3((unsigned)grid), dim3(256), true, st, codes, sf, scale, rows, (int)K,
+                 group_rows, y, ldy, vec32);
     else
-        k_dequant_nvfp4<false><<<(unsigned)grid, 256, 0, st>>>(codes, sf, scale, rows, (int)K, group_rows, y, ldy, vec32);
+        launch_k(k_dequant_nvfp4<false>, dim3((unsigned)grid), dim3(256), true, st, codes, sf, scale, rows, (int)K,
+                 group_rows, y, ldy, vec32);
 }
 
 }  // namespace bsq
