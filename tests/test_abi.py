@@ -83,3 +83,27 @@ def test_moe_workspace_layout_is_consistent(lib):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert L.h - L.xq_codes >= L.capacity * (H // 2 + H // 16 + 4)
     assert L.total == bsq.moe_workspace_size(T, H, I, E, k) and L.total > L.scan
+
+
+def test_host_validation_of_dequantize_and_2d_without_a_gpu(lib):
+    P = ctypes.c_void_p
+    d = P(4096)
+    # dequantize_nvfp4(codes, sf, scale, rows, K, group_rows, y, ldy, flags, status, stream)
+    assert lib.dequantize_nvfp4(d, d, d, 8, 256, 1, d, 256, 1 << 5, None, None) == 4  # flags
+    assert lib.dequantize_nvfp4(d, d, d, 8, 250, 1, d, 256, 0, None, None) == 2       # K % 16
+    assert lib.dequantize_nvfp4(d, d, d, 8, 256, 1, d, 128, 0, None, None) == 2       # ldy < K
+    assert lib.dequantize_nvfp4(d, d, d, 8, 256, 0, d, 256, 0, None, None) == 2       # group_rows
+    assert lib.dequantize_nvfp4(None, d, d, 8, 256, 1, d, 256, 0, None, None) == 1    # null
+    assert lib.dequantize_nvfp4(d, d, d, 8, 256, 1, P(4104), 256, 0, None, None) == 3  # y alignment
+    assert lib.dequantize_nvfp4(d, d, d, 8, 256, 1, d, 260, 0, None, None) == 3       # ldy % 8
+    assert lib.dequantize_nvfp4(d, P(4097), d, 8, 256, 1, d, 256, 0, None, None) == 3  # sf alignment
+    assert lib.dequantize_nvfp4(d, d, d, 0, 256, 1, d, 256, 0, None, None) == 0       # empty: no-op
+    # quantize_nvfp4_2d(x, rows, K, codes, sf, codes_t, sf_t, scale, flags, status, stream)
+    assert lib.quantize_nvfp4_2d(d, 32, 256, d, d, d, d, d, 1, None, None) == 4        # flags
+    assert lib.quantize_nvfp4_2d(d, 24, 256, d, d, d, d, d, 0, None, None) == 2        # rows % 16
+    assert lib.quantize_nvfp4_2d(d, 32, 248, d, d, d, d, d, 0, None, None) == 2        # K % 16
+    assert lib.quantize_nvfp4_2d(d, 32, 256, d, d, d, None, d, 0, None, None) == 1     # transposed pair half given
+    assert lib.quantize_nvfp4_2d(d, 32, 256, d, d, None, None, None, 0, None, None) == 1  # no scale
+    assert lib.quantize_nvfp4_2d(P(4100), 32, 256, d, d, d, d, d, 0, None, None) == 3  # x alignment
+    assert lib.quantize_nvfp4_2d(d, 32, 256, d, d, P(4100), d, d, 0, None, None) == 3  # codes_t alignment
+    assert lib.quantize_nvfp4_2d(d, 0, 256, d, d, d, d, d, 0, None, None) == 0         # empty: no-op
