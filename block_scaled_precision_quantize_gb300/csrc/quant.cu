@@ -489,6 +489,7 @@ __global__ void __launch_bounds__(256) k_requant_colmax(const uint8_t* __restric
                                                         const float* __restrict__ row_scale, int64_t rows, int64_t K,
                                                         unsigned int* __restrict__ colmax)
 {
+    pdl_enter();
     __shared__ float red[8][RQ1_COLS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t c0 = (int64_t)blockIdx.x * RQ1_COLS + 32 * (lane & 7);
@@ -614,6 +615,7 @@ __global__ void __launch_bounds__(256) k_requant_main(const uint8_t* __restrict_
                                                       float* __restrict__ nv_scale, uint8_t* __restrict__ mx_codes,
                                                       uint8_t* __restrict__ mx_sf, const PhiloxKeys keys)
 {
+    pdl_enter();
     extern __shared__ __align__(16) float DT[];  // [RQ_TK][RQ_TM]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t m0 = (int64_t)blockIdx.y * RQ_TM, k0 = (int64_t)blockIdx.x * RQ_TK;
@@ -795,16 +797,17 @@ __global__ void k_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, i
 // next one's launch; the MoE forward launches plainly (there the GEMM's
 // CTAs need the SMs to themselves).
 template <typename... KArgs, typename... Args>
-static void launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, bool pdl, cudaStream_t st, Args... args)
+static void launch_ks(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t st,
+                      Args... args)
 {
     if (!pdl) {
-        kernel<<<grid, block, 0, st>>>(args...);
+        kernel<<<grid, block, smem, st>>>(args...);
         return;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -812,6 +815,11 @@ static void launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, bool pdl, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+template <typename... KArgs, typename... Args>
+static void launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, bool pdl, cudaStream_t st, Args... args)
+{
+    launch_ks(kernel, grid, block, 0, pdl, st, args...);
 }
 
 static int grid_for(int64_t warps_needed, int sms)
@@ -905,8 +913,8 @@ static cudaError_t requant_main(dim3 grid, const uint8_t* codes, const uint8_t* 
                                     (int)RQ_SMEM);
     });
     if (err != cudaSuccess) return err;
-    k_requant_main<S, R, N, M><<<grid, 256, RQ_SMEM, st>>>(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc,
-                                                            mxs, philox_keys(seed));
+    launch_ks(k_requant_main<S, R, N, M>, grid, dim3(256), RQ_SMEM, true, st, codes, sf, row_scale, rows, K, colmax,
+              nvc, nvs, nvt, mxc, mxs, philox_keys(seed));
     return cudaGetLastError();
 }
 
@@ -919,8 +927,8 @@ static cudaError_t requant_passes(const uint8_t* codes, const uint8_t* sf, const
         cudaError_t err = cudaMemsetAsync(colmax, 0, (size_t)K * sizeof(unsigned int), st);
         if (err != cudaSuccess) return err;
         dim3 g1((unsigned)((K + RQ1_COLS - 1) / RQ1_COLS), (unsigned)((rows + RQ1_ROWS - 1) / RQ1_ROWS));
-        if (swz) k_requant_colmax<true><<<g1, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
-        else k_requant_colmax<false><<<g1, 256, 0, st>>>(codes, sf, row_scale, rows, K, colmax);
+        if (swz) launch_k(k_requant_colmax<true>, g1, dim3(256), true, st, codes, sf, row_scale, rows, K, colmax);
+        else launch_k(k_requant_colmax<false>, g1, dim3(256), true, st, codes, sf, row_scale, rows, K, colmax);
     }
     dim3 g2((unsigned)((K + RQ_TK - 1) / RQ_TK), (unsigned)((rows + RQ_TM - 1) / RQ_TM));
 #define BSQ_RQ(S, R, N, M) \
