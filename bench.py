@@ -529,6 +529,14 @@ def quantizer_components(bsq, synth, dev, P):
                                    bsq.SF_SWIZZLED, None, st)
 
     record("nvfp4_per_token_16384x2048", time_rotating(nv, n, 10 * n) * 1e3, b, n)
+
+    def nr(i):
+        x, codes, sf, t = sets[i % n]
+        L.quantize_nvfp4_rht(x.data_ptr(), 16384, 2048, 2048, 7, codes.data_ptr(), sf.data_ptr(), t.data_ptr(),
+                             bsq.SF_SWIZZLED, None, st)
+
+    # the same with the 32-point random Hadamard transform in front (same bytes)
+    record("nvfp4_rht_16384x2048", time_rotating(nr, n, 10 * n) * 1e3, b, n)
     del sets
     # BF16 dequantization of NVFP4 (the dequantized backward's operands), 16384 x 2048, swizzled SF
     b = 16384 * (1024 + 128 + 4) + 16384 * 2048 * 2

@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "load", "build", "BsqError",
     "quantize_nvfp4_per_token", "quantize_nvfp4_per_expert", "quantize_mxfp8_rowcol",
-    "quantize_nvfp4_2d", "dequantize_nvfp4", "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
+    "quantize_nvfp4_2d", "quantize_nvfp4_rht", "dequantize_nvfp4", "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
     "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes",
     "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
@@ -59,6 +59,7 @@ _SIGS = {
     "quantize_mxfp8_rowcol": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _U32, _P, _P]),
     "dequantize_nvfp4": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _I64, _U32, _P, _P]),
     "quantize_nvfp4_2d": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _U32, _P, _P]),
+    "quantize_nvfp4_rht": (ctypes.c_int, [_P, _I64, _I64, _I64, _U64, _P, _P, _P, _U32, _P, _P]),
     "bsq_requant_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "requant_transpose_sr": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _U64, _P, _SZ, _U32,
                                             _P, _P]),
@@ -193,6 +194,20 @@ def quantize_mxfp8_rowcol(x, row=True, col=True, swizzled=False, dev_status=None
                                         SF_SWIZZLED if swizzled else 0, _ptr(dev_status), _stream(dev)),
            "quantize_mxfp8_rowcol")
     return rc, rs, cc, cs
+
+
+def quantize_nvfp4_rht(x, seed=0, swizzled=False, dev_status=None):
+    """Per-token NVFP4 of the 32-point random Hadamard transform of each row of
+    bf16 x [rows, K] (K % 32 == 0): (codes [rows, K/2], sf, row_scale [rows])."""
+    _cuda(x, "x")
+    rows, K = x.shape
+    codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
+    sf = _sf_alloc(rows, K // 16, swizzled, x.device)
+    scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(load().quantize_nvfp4_rht(_ptr(x), rows, K, K, int(seed), _ptr(codes), _ptr(sf), _ptr(scale),
+                                     SF_SWIZZLED if swizzled else 0, _ptr(dev_status), _stream(x.device)),
+           "quantize_nvfp4_rht")
+    return codes, sf, scale
 
 
 def quantize_nvfp4_2d(x, transposed=True, dev_status=None):

@@ -109,6 +109,23 @@ bsq_status quantize_nvfp4_per_token(const void* x, int64_t rows, int64_t K, int6
     return launched();
 }
 
+bsq_status quantize_nvfp4_rht(const void* x, int64_t rows, int64_t K, int64_t ldx, uint64_t seed, uint8_t* codes,
+                              uint8_t* sf, float* row_scale, uint32_t flags, int32_t* dev_status, bsq_stream_t stream)
+{
+    (void)dev_status;
+    if (flags & ~BSQ_SF_SWIZZLED) return BSQ_ERR_FLAGS;
+    if (rows < 0 || K <= 0 || K % 32 != 0 || K > 65536 || ldx < K || rows > (int64_t)1 << 31) return BSQ_ERR_SHAPE;
+    if (rows == 0) return BSQ_OK;
+    if (!x || !codes || !sf || !row_scale) return BSQ_ERR_NULL;
+    if (!a16(x) || !a16(codes) || ldx % 8 != 0) return BSQ_ERR_ALIGN;
+    int sms;
+    bsq_status st = current_device(&sms);
+    if (st != BSQ_OK) return st;
+    launch_nvfp4_rht(static_cast<const uint16_t*>(x), rows, K, ldx, seed, codes, sf, row_scale,
+                     (flags & BSQ_SF_SWIZZLED) != 0, sms, stream);
+    return launched();
+}
+
 bsq_status quantize_nvfp4_2d(const void* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf_tiles,
                              uint8_t* codes_t, uint8_t* sf_tiles_t, float* tensor_scale, uint32_t flags,
                              int32_t* dev_status, bsq_stream_t stream)

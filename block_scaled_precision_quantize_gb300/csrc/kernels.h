@@ -12,6 +12,8 @@ void launch_nvfp4_rows(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, 
 void launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t rows_per_group, float* group_amax,
                        int sms, cudaStream_t st);
 void launch_group_finalize(float* scale, int64_t groups, cudaStream_t st);
+void launch_nvfp4_rht(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint64_t seed, uint8_t* codes,
+                      uint8_t* sf, float* row_scale, bool swz, int sms, cudaStream_t st);
 cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf,
                             uint8_t* codes_t, uint8_t* sf_t, float* tscale, int sms, cudaStream_t st);
 void launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* sf, const float* scale, int64_t rows, int64_t K,

@@ -1019,6 +1019,132 @@ cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, cons
     return requant_passes(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, sr, swz, st);
 }
 
+// ---------------------------------------------------------------- RHT + NVFP4
+// Per-token NVFP4 of a 32-point random Hadamard transform of each row
+// ("End-to-End 4-Bit Training", section "第三个决定": the transform spreads
+// outliers over their group before block quantization).  Per group of 32
+// consecutive elements, y = H32 (s . x) with the Sylvester matrix unnormalized,
+// in binary32 by the butterfly h = 1, 2, 4, 8, 16; s = the 32 bits of word 0
+// of Philox4x32-10(seed, (0, 0, 2, 0)) (bit j set: s_j = -1).  One warp per
+// row; lane l holds the 16-element blocks l, l + 32, ... of a chunk of 128
+// blocks, so a block's group partner (block b ^ 1) sits in lane l ^ 1 at the
+// same register slot: stages 1-8 run in registers, stage 16 is one shuffle.
+// Rows of up to 128 blocks are quantized from registers; longer rows take two
+// passes over their chunks (the transformed row's maximum, then the encode).
+namespace {
+
+BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int c0, int lane, uint32_t signs,
+                           float (&v)[4][16], int nb)
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int b = c0 + lane + 32 * i;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
+        if (i < nb && b < nblk) {
+            a = ldg_stream(xr + 16 * b);
+            c = ldg_stream(xr + 16 * b + 8);
+        }
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        const uint32_t sg = (lane & 1) ? (signs >> 16) : signs;  // this block's half of the group
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+            v[i][2 * j] = ((sg >> (2 * j)) & 1u) ? -lo : lo;
+            v[i][2 * j + 1] = ((sg >> (2 * j + 1)) & 1u) ? -hi : hi;
+        }
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if ((j & h) == 0) {
+                    const float p = v[i][j], q = v[i][j + h];
+                    v[i][j] = __fadd_rn(p, q);
+                    v[i][j + h] = __fsub_rn(p, q);
+                }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i][j], 1);
+            v[i][j] = (lane & 1) ? __fsub_rn(o, v[i][j]) : __fadd_rn(v[i][j], o);
+        }
+    }
+}
+
+template <int NB, bool SWZ>
+__global__ void __launch_bounds__(256) k_nvfp4_rht(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ldx,
+                                                   uint64_t seed, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                   float* __restrict__ row_scale)
+{
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int nblk = (int)(K >> 4);
+    const int ncol_pad = SWZ ? ((nblk + 3) & ~3) : nblk;
+    const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const uint32_t signs = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32)).x;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows_iter; r += nwarps) {
+        if (r >= rows) {  // swizzle padding rows
+            for (int b = lane; b < ncol_pad; b += 32) sf[sf_swizzled(r, b, (ncol_pad + 3) >> 2)] = 0u;
+            continue;
+        }
+        const uint16_t* xr = x + r * ldx;
+        float v[4][16];
+        float amax = 0.0f;
+        for (int c0 = 0; c0 < nblk; c0 += 128) {  // one chunk for rows of up to 128 blocks
+            rht_blocks(xr, nblk, c0, lane, signs, v, NB);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        }
+        amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax)));  // non-negative: bit order
+        const float t = __fdiv_rn(amax, kNvfp4ScaleDivisor);
+        if (lane == 0) row_scale[r] = t;
+        const float six_t = __fmul_rn(6.0f, t);
+        uint2* crow = reinterpret_cast<uint2*>(codes + r * (K >> 1));
+        for (int c0 = 0; c0 < nblk; c0 += 128) {
+            if (nblk > 128) rht_blocks(xr, nblk, c0, lane, signs, v, NB);  // second pass: transform again
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int b = c0 + lane + 32 * i;
+                if (i >= NB || b >= nblk) {
+                    if (SWZ && i < NB && b < ncol_pad) sf[sf_swizzled(r, b, (ncol_pad + 3) >> 2)] = 0u;
+                    continue;
+                }
+                uint2 c = make_uint2(0u, 0u);
+                uint32_t sfb = 0u;
+                if (t != 0.0f) {
+                    float ab = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ab = fmaxf(ab, fabsf(v[i][j]));
+                    const BlockScale bs = nvfp4_block_scale(ab, six_t, t);
+                    c = encode16(v[i], bs.enc);
+                    sfb = bs.sf;
+                }
+                crow[b] = c;
+                sf[SWZ ? sf_swizzled(r, b, (ncol_pad + 3) >> 2) : r * nblk + b] = (uint8_t)sfb;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+void launch_nvfp4_rht(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint64_t seed, uint8_t* codes,
+                      uint8_t* sf, float* row_scale, bool swz, int sms, cudaStream_t st)
+{
+    const int64_t nblk = K >> 4;
+    const int64_t rows_iter = swz ? ((rows + 127) & ~(int64_t)127) : rows;
+    const dim3 grid((unsigned)grid_for(rows_iter, sms));
+    const int nb = nblk <= 32 ? 1 : nblk <= 64 ? 2 : 4;
+#define BSQ_RHT(N, S) launch_k(k_nvfp4_rht<N, S>, grid, dim3(256), true, st, x, rows, K, ldx, seed, codes, sf, row_scale)
+    if (swz) {
+        if (nb == 1) BSQ_RHT(1, true); else if (nb == 2) BSQ_RHT(2, true); else BSQ_RHT(4, true);
+    } else {
+        if (nb == 1) BSQ_RHT(1, false); else if (nb == 2) BSQ_RHT(2, false); else BSQ_RHT(4, false);
+    }
+#undef BSQ_RHT
+}
+
 // ---------------------------------------------------------------- 2-D NVFP4
 // One E4M3 scale per 16 x 16 tile and one FP32 scale per tensor ("End-to-End
 // 4-Bit Training", section "第二个决定": square block scales are the same

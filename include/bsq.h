@@ -127,6 +127,29 @@ bsq_status quantize_nvfp4_per_expert(const void* w, int64_t experts, int64_t row
                                      uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * quantize_nvfp4_rht: per-token NVFP4 of a 32-point random Hadamard transform
+ * of each row ("End-to-End 4-Bit Training", "第三个决定": a 32-dimensional
+ * random Hadamard transform spreads outliers over their group before block
+ * quantization; the page quantizes the result to a format it does not
+ * define, NVFP4 stands in).  Per group of 32 consecutive elements,
+ * y = H32 (s . x): H32 the Sylvester Hadamard matrix (entries +-1,
+ * H[i][j] = (-1)^popcount(i & j)), unnormalized (H32 H32 = 32 I inverts it),
+ * computed in binary32 by the butterfly h = 1, 2, 4, 8, 16 ((v_i, v_{i+h}) <-
+ * (v_i + v_{i+h}, v_i - v_{i+h}) for (i & h) == 0); s_j = -1 iff bit j of
+ * word 0 of Philox4x32-10(key = seed, counter = (0, 0, 2, 0)).  Then the
+ * per-token recipe of quantize_nvfp4_per_token on y (no 4/6).
+ *   x          bf16 [rows][ldx], K columns used; ldx % 8 == 0, 16-byte aligned
+ *   codes      out, [rows][K/2] (codes of y)
+ *   sf         out, E4M3 block scales of y, linear or swizzled
+ *   row_scale  out, fp32 [rows]
+ *   flags      BSQ_SF_SWIZZLED
+ * K % 32 == 0, 0 < K <= 65536; rows >= 0 (0 is a no-op).
+ * ------------------------------------------------------------------------- */
+bsq_status quantize_nvfp4_rht(const void* x, int64_t rows, int64_t K, int64_t ldx, uint64_t seed,
+                              uint8_t* codes, uint8_t* sf, float* row_scale,
+                              uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * quantize_nvfp4_2d: NVFP4 with one E4M3 scale per 16 x 16 square block and
  * one FP32 scale per tensor, emitting the row-major operand and, optionally,
  * the transposed one ("End-to-End 4-Bit Training", "第二个决定": square block

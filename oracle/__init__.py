@@ -78,6 +78,9 @@ def _declare(L):
         "bsqo_nvfp4_quantize_group": (None, [_P, _I64, _I64, _I64, _P, _P, _P]),
         "bsqo_nvfp4_dequantize": (None, [_P, _P, _P, _I64, _I64, _P]),
         "bsqo_nvfp4_quantize_2d": (None, [_P, _I64, _I64, _P, _P, _P]),
+        "bsqo_rht_signs": (_U32, [_U64]),
+        "bsqo_rht32": (None, [_P, _I64, _U32, _P]),
+        "bsqo_nvfp4_quantize_rht": (None, [_P, _I64, _I64, _U64, _P, _P, _P]),
         "bsqo_nvfp4_block_candidate": (None, [_P, ctypes.c_float, ctypes.c_float, _P, _P, _P]),
         "bsqo_sf_swizzled_offset": (_I64, [_I64, _I64, _I64]),
         "bsqo_sf_swizzle": (None, [_P, _I64, _I64, _P]),
@@ -230,6 +233,33 @@ def nvfp4_quantize_2d(x_bits: np.ndarray):
     t = np.empty(1, np.float32)
     lib().bsqo_nvfp4_quantize_2d(_ptr(x), rows, K, _ptr(codes), _ptr(sf), _ptr(t))
     return codes, sf, float(t[0])
+
+
+def rht_signs(seed: int) -> int:
+    """The 32 signs of the random Hadamard transform as a bit mask (bit j set:
+    s_j = -1), from Philox4x32-10 stream 2."""
+    return int(lib().bsqo_rht_signs(int(seed)))
+
+
+def rht32(x: np.ndarray, signs: int) -> np.ndarray:
+    """y = H32 (s . x) per 32-element group of the last axis, binary32 in the
+    butterfly order ("End-to-End 4-Bit Training", section "第三个决定")."""
+    xf = _c(x, np.float32)
+    y = np.empty_like(xf)
+    lib().bsqo_rht32(_ptr(xf), xf.size, int(signs), _ptr(y))
+    return y
+
+
+def nvfp4_quantize_rht(x_bits: np.ndarray, seed: int):
+    """Per-token NVFP4 of the 32-point random Hadamard transform of bf16 x
+    [rows, K] (K % 32 == 0): (codes [rows, K/2], sf [rows, K/16], t [rows])."""
+    x = _c(x_bits, np.uint16)
+    rows, K = x.shape
+    codes = np.empty((rows, K // 2), np.uint8)
+    sf = np.empty((rows, K // 16), np.uint8)
+    t = np.empty(rows, np.float32)
+    lib().bsqo_nvfp4_quantize_rht(_ptr(x), rows, K, int(seed), _ptr(codes), _ptr(sf), _ptr(t))
+    return codes, sf, t
 
 
 def nvfp4_dequantize_bf16(codes, sf, t_rows) -> np.ndarray:

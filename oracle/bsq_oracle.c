@@ -406,6 +406,66 @@ EXPORT void bsqo_nvfp4_quantize_2d(const uint16_t* x, int64_t rows, int64_t K,
         }
 }
 
+/* ------------------------------------------------------------------------
+ * 32-point random Hadamard transform before quantization.  [TML-ZH]
+ * "第三个决定": a 32-dimensional random Hadamard transform spreads outliers
+ * over their group before the values are block-quantized.
+ * READINGS: per group of 32 consecutive elements of a row,
+ * y = H32 (s . x), H32 the Sylvester Hadamard matrix (entries +-1,
+ * H[i][j] = (-1)^popcount(i & j)), unnormalized: the per-token FP32 scale
+ * absorbs the constant and H32 H32 = 32 I inverts it exactly.  Binary32,
+ * by the butterfly h = 1, 2, 4, 8, 16 over pairs (i, i + h) with
+ * (i & h) == 0: (v_i, v_{i+h}) <- (v_i + v_{i+h}, v_i - v_{i+h}).
+ * s: one sign vector per tensor, s_j = -1 iff bit j of word 0 of
+ * Philox4x32-10(key = seed, counter = (0, 0, 2, 0)) (stream 2: streams 0 and
+ * 1 feed stochastic rounding).  The transformed rows are quantized with the
+ * per-row recipe above (no 4/6); the pages' own target format for the
+ * transformed values is not defined, so NVFP4 stands in.
+ * ---------------------------------------------------------------------- */
+EXPORT uint32_t bsqo_rht_signs(uint64_t seed)
+{
+    uint32_t ctr[4] = {0u, 0u, 2u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    bsqo_philox4x32_10(ctr, key, out);
+    return out[0];
+}
+
+EXPORT void bsqo_rht32(const float* x, int64_t n, uint32_t signs, float* y)
+{
+    for (int64_t g = 0; g + 32 <= n; g += 32) {
+        float v[32];
+        for (int j = 0; j < 32; ++j) v[j] = ((signs >> j) & 1u) ? -x[g + j] : x[g + j];
+        for (int h = 1; h < 32; h <<= 1)
+            for (int i = 0; i < 32; ++i)
+                if ((i & h) == 0) {
+                    const float a = v[i], b = v[i + h];
+                    v[i] = a + b;
+                    v[i + h] = a - b;
+                }
+        for (int j = 0; j < 32; ++j) y[g + j] = v[j];
+    }
+}
+
+EXPORT void bsqo_nvfp4_quantize_rht(const uint16_t* x, int64_t rows, int64_t K, uint64_t seed,
+                                    uint8_t* codes, uint8_t* sf, float* t)
+{
+    if (rows <= 0 || K <= 0) return;
+    const uint32_t signs = bsqo_rht_signs(seed);
+    float* xf = (float*)malloc(sizeof(float) * (size_t)K);
+    float* y = (float*)malloc(sizeof(float) * (size_t)K);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t k = 0; k < K; ++k) xf[k] = bf16_to_f32(x[r * K + k]);
+        bsqo_rht32(xf, K, signs, y);
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) amax = fmaxf(amax, fabsf(y[k]));
+        t[r] = nvfp4_scale_from_amax(amax);
+        nvfp4_row_given_t(y, K, t[r], 0, codes + r * (K / 2), sf + r * (K / 16));
+    }
+    free(xf);
+    free(y);
+}
+
 /* Step 5 above: binary32 dequantization of an NVFP4 tensor (per-row t). */
 EXPORT void bsqo_nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float* t,
                                   int64_t rows, int64_t K, float* out)

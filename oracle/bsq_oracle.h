@@ -65,6 +65,12 @@ void bsqo_mxfp8_quantize_rowcol(const uint16_t* x, int64_t rows, int64_t K, int6
 void bsqo_nvfp4_quantize_2d(const uint16_t* x, int64_t rows, int64_t K,
                             uint8_t* codes, uint8_t* sf_tiles, float* t_out);
 
+/* 32-point random Hadamard transform, and per-token NVFP4 of the transformed rows */
+uint32_t bsqo_rht_signs(uint64_t seed);
+void bsqo_rht32(const float* x, int64_t n, uint32_t signs, float* y);
+void bsqo_nvfp4_quantize_rht(const uint16_t* x, int64_t rows, int64_t K, uint64_t seed,
+                             uint8_t* codes, uint8_t* sf, float* t);
+
 /* backward dequantize -> transpose -> requantize */
 void bsqo_requant_transpose(const uint8_t* codes, const uint8_t* sf, const float* t,
                             int64_t rows, int64_t K, int sr, uint64_t seed,

@@ -455,3 +455,58 @@ def test_2d_one_outlier_flushes_its_tile(O):
 def test_2d_zero_tensor(O):
     c, s, t = O.nvfp4_quantize_2d(np.zeros((32, 48), np.uint16))
     assert t == 0.0 and not c.any() and not s.any()
+
+
+# ---------------------------------------------------------------- 32-point random Hadamard transform
+def _hadamard32():
+    import scipy.linalg
+    return scipy.linalg.hadamard(32).astype(np.float64)  # Sylvester construction
+
+
+def test_rht_unit_vectors_give_hadamard_columns(O):
+    H = _hadamard32()
+    signs = O.rht_signs(7)
+    s = np.where((signs >> np.arange(32)) & 1, -1.0, 1.0)
+    for k in range(32):
+        e = np.zeros(32, np.float32)
+        e[k] = 1.0
+        np.testing.assert_array_equal(O.rht32(e, 0), H[:, k])
+        np.testing.assert_array_equal(O.rht32(e, signs), s[k] * H[:, k])
+
+
+def test_rht_exact_on_small_integers_and_inverts(O):
+    # integer inputs up to 8 keep every butterfly sum exact in binary32, so the
+    # transform equals H (s . x) in float64, and H H = 32 I undoes it
+    rng = np.random.default_rng(3)
+    x = rng.integers(-8, 9, size=(4, 96)).astype(np.float32)
+    signs = O.rht_signs(11)
+    s = np.where((signs >> np.arange(32)) & 1, -1.0, 1.0)
+    y = O.rht32(x, signs)
+    ref = (x.reshape(-1, 32).astype(np.float64) * s) @ _hadamard32().T
+    np.testing.assert_array_equal(y.reshape(-1, 32), ref)
+    back = O.rht32(y, 0).reshape(-1, 32) * s / 32.0
+    np.testing.assert_array_equal(back.reshape(x.shape), x)
+
+
+def test_rht_binary32_rounding_bound(O):
+    # arbitrary values: five binary32 additions per output, so each output is
+    # within 5 * 2^-24 * sum|x| of the exact transform
+    x = synth.bf16_bits_to_f32(synth.normal_with_outliers(8, 256, seed=4)).astype(np.float32)
+    signs = O.rht_signs(5)
+    s = np.where((signs >> np.arange(32)) & 1, -1.0, 1.0)
+    y = O.rht32(x, signs).reshape(-1, 32).astype(np.float64)
+    g = x.reshape(-1, 32).astype(np.float64)
+    exact = (g * s) @ _hadamard32().T
+    bound = 5 * 2.0 ** -24 * np.abs(g).sum(axis=1, keepdims=True)
+    assert (np.abs(y - exact) <= bound).all()
+
+
+def test_rht_quantization_is_the_per_row_recipe_of_the_transform(O):
+    x = synth.normal_with_outliers(16, 128, seed=6)
+    c, s, t = O.nvfp4_quantize_rht(x, seed=9)
+    y = O.rht32(synth.bf16_bits_to_f32(x).astype(np.float32), O.rht_signs(9))
+    t_ref = (np.abs(y).max(axis=1) / np.float32(2688.0)).astype(np.float32)
+    np.testing.assert_array_equal(t, t_ref)
+    c2, s2 = O.nvfp4_quantize_rows_given_t(y, t_ref)
+    np.testing.assert_array_equal(c, c2)
+    np.testing.assert_array_equal(s, s2)
