@@ -87,6 +87,7 @@ def _declare(L):
         "bsqo_mxfp8_quantize_rowcol": (None, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
         "bsqo_requant_transpose": (None, [_P, _P, _P, _I64, _I64, _INT, _U64, _P, _P, _P, _P, _P]),
         "bsqo_gemm_nvfp4": (None, [_P, _P, _P, _I64, _I64, _P, _P, ctypes.c_float, _I64, _P, _P]),
+        "bsqo_gemm_mxfp8": (None, [_P, _P, _P, _I64, _I64, _P, _P, ctypes.c_float, _I64, _P, _P]),
         "bsqo_gemm_nvfp4_sampled": (None, [_P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _I64, _P, _P]),
         "bsqo_route": (_I64, [_P, _I64, _I64, _I64, _I64, _P, _P, _P]),
         "bsqo_swiglu": (None, [_P, _I64, _I64, _P]),
@@ -341,6 +342,24 @@ def gemm_nvfp4(a_codes, a_sf, a_t, b_codes, b_sf, b_t: float, with_abs: bool = T
     ab = np.empty((M, N), np.float64) if with_abs else None
     lib().bsqo_gemm_nvfp4(_ptr(a_codes), _ptr(a_sf), _ptr(a_t), M, K, _ptr(b_codes), _ptr(b_sf),
                           float(b_t), N, _ptr(out), _ptr(ab))
+    return out, ab
+
+
+def gemm_mxfp8(a_codes, a_sf, a_t, b_codes, b_sf, b_t: float = 1.0, with_abs: bool = True):
+    """fp64 GEMM on exactly dequantized MXFP8 operands (codes [rows, K] E4M3,
+    SF [rows, K/32] E8M0 linear): out[m, n] = sum_k A[m, k] * B[n, k].
+    Returns (out, sum_k |A*B|)."""
+    a_codes = _c(a_codes, np.uint8)
+    a_sf = _c(a_sf, np.uint8)
+    a_t = _c(a_t, np.float32)
+    b_codes = _c(b_codes, np.uint8)
+    b_sf = _c(b_sf, np.uint8)
+    M, K = a_codes.shape
+    N = b_codes.shape[0]
+    out = np.empty((M, N), np.float64)
+    ab = np.empty((M, N), np.float64) if with_abs else None
+    lib().bsqo_gemm_mxfp8(_ptr(a_codes), _ptr(a_sf), _ptr(a_t), M, K, _ptr(b_codes), _ptr(b_sf), float(b_t), N,
+                          _ptr(out), _ptr(ab))
     return out, ab
 
 

@@ -676,6 +676,42 @@ EXPORT void bsqo_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const f
     free(bd);
 }
 
+/* GEMM on exactly dequantized MXFP8 operands (fp64): out[m][n] =
+ * sum_k A[m][k] B[n][k], A and B K-major, each element E4M3(code) *
+ * 2^(E8M0(sf of its 32-block) - 127) ([MILES-IT] "Il supporto Miles ...":
+ * the MXFP8 recipe also runs the weight- and data-gradient GEMMs in MXFP8;
+ * [LMSYS] "Recipe 1: End-to-end MXFP8").  a_t / b_t (FP32) multiply the rows
+ * of A and all of B (1 for plain MXFP8).  SF linear [rows][K/32]. */
+static double mx_deq64(const uint8_t* codes, const uint8_t* sf, int64_t r, int64_t k, int64_t K)
+{
+    return (double)bsqo_e4m3_decode(codes[r * K + k]) * (double)bsqo_e8m0_decode(sf[r * (K / 32) + k / 32]);
+}
+
+EXPORT void bsqo_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_t, int64_t M, int64_t K,
+                            const uint8_t* b_codes, const uint8_t* b_sf, float b_t, int64_t N,
+                            double* out, double* abs_out)
+{
+    double* bd = (double*)malloc(sizeof(double) * (size_t)(N * K));
+    double* ad = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) bd[n * K + k] = mx_deq64(b_codes, b_sf, n, k, K) * (double)b_t;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) ad[k] = mx_deq64(a_codes, a_sf, m, k, K) * (double)a_t[m];
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = ad[k] * bd[n * K + k];
+                acc += p;
+                aacc += fabs(p);
+            }
+            out[m * N + n] = acc;
+            if (abs_out) abs_out[m * N + n] = aacc;
+        }
+    }
+    free(ad);
+    free(bd);
+}
+
 /* One output element per sample: row a_rows[s] of A against row b_rows[s]
  * of B (B rows of all groups stacked), with B's FP32 scale b_t[b_group[s]]. */
 EXPORT void bsqo_gemm_nvfp4_sampled(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_t,

@@ -56,6 +56,11 @@ void bsqo_nvfp4_dequantize(const uint8_t* codes, const uint8_t* sf, const float*
 int64_t bsqo_sf_swizzled_offset(int64_t row, int64_t kblock, int64_t K);
 void bsqo_sf_swizzle(const uint8_t* sf, int64_t rows, int64_t cols, uint8_t* out);
 
+/* GEMM on exactly dequantized MXFP8 operands (fp64) */
+void bsqo_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_t, int64_t M, int64_t K,
+                     const uint8_t* b_codes, const uint8_t* b_sf, float b_t, int64_t N,
+                     double* out, double* abs_out);
+
 /* MXFP8 quantization */
 void bsqo_mxfp8_quantize_rowcol(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx,
                                 uint8_t* row_codes, uint8_t* row_sf,

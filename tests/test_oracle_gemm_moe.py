@@ -110,3 +110,42 @@ def test_combine_closed_forms(O):
     ref = 0.5 * of[slot_of.reshape(T, k)].sum(axis=1)
     yf = synth.bf16_bits_to_f32(y).astype(np.float64)
     assert np.all(np.abs(yf - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-38)
+
+
+# ---------------------------------------------------------------- MXFP8 GEMM (the backward's operands)
+def _mx_deq64(codes, sf):
+    """Independent fp64 decode of MXFP8: E4M3 via torch, E8M0 as 2^(b - 127)."""
+    c = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    s = np.exp2(np.asarray(sf, np.float64) - 127.0)
+    return c * np.repeat(s, 32, axis=-1)
+
+
+def test_mxfp8_gemm_matches_numpy_fp64(O):
+    a = synth.rows_log_uniform_std(64, 256, seed=3)
+    w = synth.normal((48, 256), seed=4, std=0.02)
+    ac, asf, _, _ = O.mxfp8_quantize_rowcol(a, col=False)
+    wc, wsf, _, _ = O.mxfp8_quantize_rowcol(w, col=False)
+    ones = np.ones(64, np.float32)
+    out, ab = O.gemm_mxfp8(ac, asf, ones, wc, wsf, 1.0)
+    A, B = _mx_deq64(ac, asf), _mx_deq64(wc, wsf)
+    ref = A @ B.T
+    assert np.all(np.abs(out - ref) <= 1e-12 * (np.abs(A) @ np.abs(B).T) + 1e-300)
+    np.testing.assert_allclose(ab, np.abs(A) @ np.abs(B).T, rtol=1e-12)
+
+
+def test_mxfp8_gemm_integer_exact_case(O):
+    # E4M3 codes of small integers (0x38 = 1, 0x40 = 2, 0x44 = 3, 0xC0 = -2) and
+    # unit block scales (E8M0 127): the sums are exact integers
+    rng = np.random.default_rng(5)
+    vals = np.array([0x00, 0x38, 0x40, 0x44, 0xC0], np.uint8)
+    ints = np.array([0, 1, 2, 3, -2], np.float64)
+    ia = rng.integers(0, 5, size=(16, 64))
+    ib = rng.integers(0, 5, size=(8, 64))
+    sa = np.full((16, 2), 127, np.uint8)
+    sb = np.full((8, 2), 127, np.uint8)
+    out, _ = O.gemm_mxfp8(vals[ia], sa, np.ones(16, np.float32), vals[ib], sb, 1.0)
+    np.testing.assert_array_equal(out, ints[ia] @ ints[ib].T)
+    # block scale 2^1 on A's second block of 32 doubles exactly that half's share
+    sa[:, 1] = 128
+    out2, _ = O.gemm_mxfp8(vals[ia], sa, np.ones(16, np.float32), vals[ib], sb, 1.0)
+    np.testing.assert_array_equal(out2, ints[ia][:, :32] @ ints[ib][:, :32].T + 2 * ints[ia][:, 32:] @ ints[ib][:, 32:].T)
