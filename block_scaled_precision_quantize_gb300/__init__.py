@@ -19,7 +19,8 @@ from . import build as _build
 __all__ = [
     "load", "build", "BsqError",
     "quantize_nvfp4_per_token", "quantize_nvfp4_per_expert", "quantize_mxfp8_rowcol",
-    "quantize_nvfp4_2d", "quantize_nvfp4_rht", "dequantize_nvfp4", "requant_transpose_sr", "grouped_expert_gemm_fp4", "moe_expert_forward",
+    "quantize_nvfp4_2d", "quantize_nvfp4_rht", "dequantize_nvfp4", "requant_transpose_sr",
+    "grouped_expert_gemm_fp4", "grouped_expert_gemm_mxfp8", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
     "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes",
     "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
@@ -65,6 +66,8 @@ _SIGS = {
                                             _P, _P]),
     "grouped_expert_gemm_fp4": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _I32, _P,
                                                _I64, _U32, _P, _P]),
+    "grouped_expert_gemm_mxfp8": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _I32, _P,
+                                                 _I64, _U32, _P, _P]),
     "bsq_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
     "bsq_moe_workspace_layout": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, ctypes.POINTER(MoeLayout)]),
     "moe_expert_forward": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -310,6 +313,31 @@ def grouped_expert_gemm_fp4(a_codes, a_sf, a_scale, offsets, b_codes, b_sf, b_sc
                                           _ptr(b_codes), _ptr(b_sf), _ptr(b_scale), epilogue, _ptr(out),
                                           out.stride(0), SF_SWIZZLED, _ptr(dev_status), _stream(a_codes.device)),
            "grouped_expert_gemm_fp4")
+    return out
+
+
+def grouped_expert_gemm_mxfp8(a_codes, a_sf, offsets, b_codes, b_sf, a_scale=None, b_scale=None,
+                              epilogue=EPI_F32, out=None, dev_status=None):
+    """Grouped block-scaled GEMM on MXFP8 operands: a_codes [M, K] E4M3
+    (expert-sorted rows, segments given by int32 offsets [E+1], multiples of
+    128), b_codes [E, N, K]; E8M0 SF swizzled.  a_scale [M] / b_scale [E]
+    default to ones.  Returns out [M, N] (fp32 or bf16)."""
+    for t, n in ((a_codes, "a_codes"), (b_codes, "b_codes"), (offsets, "offsets")):
+        _cuda(t, n)
+    M, K = a_codes.shape
+    E, N = b_codes.shape[0], b_codes.shape[1]
+    dev = a_codes.device
+    if a_scale is None:
+        a_scale = torch.ones(M, dtype=torch.float32, device=dev)
+    if b_scale is None:
+        b_scale = torch.ones(E, dtype=torch.float32, device=dev)
+    dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty(M, N, dtype=dt, device=dev)
+    _check(load().grouped_expert_gemm_mxfp8(_ptr(a_codes), _ptr(a_sf), _ptr(a_scale), _ptr(offsets), E, M, K, N,
+                                            _ptr(b_codes), _ptr(b_sf), _ptr(b_scale), epilogue, _ptr(out),
+                                            out.stride(0), SF_SWIZZLED, _ptr(dev_status), _stream(dev)),
+           "grouped_expert_gemm_mxfp8")
     return out
 
 

@@ -295,6 +295,47 @@ bsq_status requant_transpose_sr_noalloc(const uint8_t* codes, const uint8_t* sf,
     return launched();
 }
 
+bsq_status grouped_expert_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                     const int32_t* offsets, int64_t experts, int64_t m_capacity, int64_t K, int64_t N,
+                                     const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,
+                                     int32_t epilogue, void* out, int64_t ldo, uint32_t flags, int32_t* dev_status,
+                                     bsq_stream_t stream)
+{
+    if (flags != 0 && flags != BSQ_SF_SWIZZLED) return BSQ_ERR_FLAGS;
+    if (epilogue != BSQ_EPI_F32 && epilogue != BSQ_EPI_BF16) return BSQ_ERR_FLAGS;
+    if (experts <= 0 || m_capacity < 0 || K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return BSQ_ERR_SHAPE;
+    if (ldo < N) return BSQ_ERR_SHAPE;
+    if (m_capacity > ((int64_t)1 << 31) - 256 || experts * N > ((int64_t)1 << 31) - 256 || K > ((int64_t)1 << 20))
+        return BSQ_ERR_SHAPE;
+    if (m_capacity == 0) return BSQ_OK;
+    if (!a_codes || !a_sf || !a_scale || !offsets || !b_codes || !b_sf || !b_scale || !out) return BSQ_ERR_NULL;
+    const int64_t esz = epilogue == BSQ_EPI_F32 ? 4 : 2;
+    if (!a16(a_codes) || !a16(b_codes) || !a16(a_sf) || !a16(b_sf) || !a16(out) || (ldo * esz) % 16 != 0)
+        return BSQ_ERR_ALIGN;
+    int sms;
+    bsq_status st = current_device(&sms);
+    if (st != BSQ_OK) return st;
+    GemmArgs g;
+    g.a_codes = a_codes;
+    g.a_sf = a_sf;
+    g.a_scale = a_scale;
+    g.offsets = offsets;
+    g.experts = experts;
+    g.m_capacity = m_capacity;
+    g.K = K;
+    g.N = N;
+    g.b_codes = b_codes;
+    g.b_sf = b_sf;
+    g.b_scale = b_scale;
+    g.epilogue = epilogue;
+    g.out = out;
+    g.ldo = ldo;
+    g.dev_status = dev_status;
+    g.sms = sms;
+    g.fmt = 1;
+    return launch_gemm_fp4(g, stream) == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
 bsq_status grouped_expert_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
                                    const int32_t* offsets, int64_t experts, int64_t m_capacity, int64_t K, int64_t N,
                                    const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,

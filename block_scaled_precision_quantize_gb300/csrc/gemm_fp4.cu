@@ -96,6 +96,15 @@ static_assert(GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES + 2048 <= 232448, "stage ri
 // K-major, no negation, N>>3 at bit 17, M = 128 (M>>4 at bit 24), scale type
 // UE4M3 (bit 23 = 0), scale-factor ids 0, dense, K = 64.
 __host__ __device__ constexpr uint32_t gm_idesc(uint32_t n) { return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24); }
+// kind::mxf8f6f4 with scale_vec::1X (the MXFP8 operands of the backward
+// GEMMs): A and B E4M3 (format 0), scale type UE8M0 (bit 23), M = 128,
+// K = 32.  Each tensor-memory scale column holds four E8M0 bytes of a row,
+// those of four consecutive 32-element blocks; the byte an MMA reads is its
+// scale-factor id (B's at bits 4-5, A's at bits 29-30).
+__host__ __device__ constexpr uint32_t gm_idesc_mx8(uint32_t n, uint32_t sf_id)
+{
+    return (sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) | (sf_id << 29);
+}
 
 // ------------------------------------------------------------------ PTX
 BSQ_DEVICE uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -165,6 +174,18 @@ BSQ_DEVICE uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32
 BSQ_DEVICE void tc_cp_sf(uint32_t taddr, uint64_t sdesc)
 {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+BSQ_DEVICE void tc_mma_mx8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
 }
 
 BSQ_DEVICE void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
@@ -335,8 +356,12 @@ struct TileInfo {
 };
 
 // EPI is the epilogue (BSQ_EPI_*): one instantiation per epilogue keeps each
-// one's register allocation to its own path.
-template <int EPI>
+// one's register allocation to its own path.  FMT is the operand format:
+// 0 NVFP4 (E2M1 codes, E4M3 scale per 16, kind::mxf4nvf4, K = 64 per MMA,
+// four 512-byte scale chunks per 128 rows and stage), 1 MXFP8 (E4M3 codes,
+// E8M0 scale per 32, kind::mxf8f6f4, K = 32 per MMA, one chunk per 128 rows
+// and stage).  A stage is 128 bytes of every row in both.
+template <int EPI, int FMT = 0>
 __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
     k_gemm_fp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmOut,
@@ -410,8 +435,9 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
     __syncthreads();
 
     constexpr bool swiglu = EPI == BSQ_EPI_SWIGLU_BF16;
-    const int k64_total = p.K >> 6;
-    const int kt_count = (k64_total + 3) >> 2;
+    const int kmma_total = FMT ? (p.K >> 5) : (p.K >> 6);  // MMAs along K (64 or 32 elements each)
+    const int kt_count = (kmma_total + 3) >> 2;
+    const int sf_chunks = FMT ? (p.K >> 7) : (p.K >> 6);  // 512-byte scale chunks per 128-row tile
     const int m_tiles = s_bad ? 0 : (off(E) + 127) >> 7;
     const int total_tiles = m_tiles * p.n_tiles;
 
@@ -438,7 +464,7 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
             uint32_t it = 0;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
                 const TileInfo t = tile_info(tile);
-                const uint8_t* sfa_src = p.a_sf + ((size_t)(t.m0 >> 7) * k64_total) * 512;
+                const uint8_t* sfa_src = p.a_sf + ((size_t)(t.m0 >> 7) * sf_chunks) * 512;
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = (int)(it % GM_STAGES);
                     const uint32_t ph = (it / GM_STAGES) & 1u;
@@ -448,16 +474,22 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
                         break;
                     }
                     const uint32_t st = sbase + (uint32_t)s * GM_STAGE_BYTES;
-                    const int nk = min(4, k64_total - 4 * kt);
+                    const int nk = min(4, kmma_total - 4 * kt);
                     // the scale factors first, on their own barrier, so the SF warps can
                     // move them into tensor memory while the codes are still arriving;
                     // boxes always deliver their full size (out-of-range parts are zero-filled)
-                    mbar_expect_tx(sf_full(s), 4096u + (uint32_t)nk * 512u);
-                    if (swiglu)
-                        tma_load_3d(st + GM_SFB_OFF, &tmSFB, kt * 256, t.nt, 2 * t.e, sf_full(s));
-                    else
-                        tma_load_2d(st + GM_SFB_OFF, &tmSFB, kt * 256, (t.e * p.N + t.nt * 256) >> 7, sf_full(s));
-                    bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 2048, (uint32_t)nk * 512u, sf_full(s));
+                    if constexpr (FMT == 1) {  // one chunk for A, one per B row tile
+                        mbar_expect_tx(sf_full(s), 1024u + 512u);
+                        tma_load_2d(st + GM_SFB_OFF, &tmSFB, kt * 64, (t.e * p.N + t.nt * 256) >> 7, sf_full(s));
+                        bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 512, 512u, sf_full(s));
+                    } else {
+                        mbar_expect_tx(sf_full(s), 4096u + (uint32_t)nk * 512u);
+                        if (swiglu)
+                            tma_load_3d(st + GM_SFB_OFF, &tmSFB, kt * 256, t.nt, 2 * t.e, sf_full(s));
+                        else
+                            tma_load_2d(st + GM_SFB_OFF, &tmSFB, kt * 256, (t.e * p.N + t.nt * 256) >> 7, sf_full(s));
+                        bulk_load(st + GM_SFA_OFF, sfa_src + (size_t)kt * 2048, (uint32_t)nk * 512u, sf_full(s));
+                    }
                     mbar_expect_tx(full_bar(s), 16384u + 32768u);
                     tma_load_2d(st + GM_A_OFF, &tmA, kt * 128, t.m0, full_bar(s));
                     if (swiglu)
@@ -487,7 +519,8 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
                 // only the tile's width matters here (no expert lookup: shared-memory
                 // loads from this thread are slow while the copies stream in)
                 const int nt = tile % p.n_tiles;
-                const uint32_t idesc = gm_idesc((swiglu || nt * 256 + 128 < p.N) ? 256u : 128u);
+                const uint32_t n_w = (swiglu || nt * 256 + 128 < p.N) ? 256u : 128u;
+                const uint32_t idesc = FMT ? gm_idesc_mx8(n_w, 0u) : gm_idesc(n_w);
                 // the epilogue has taken the previous accumulator out of tensor memory
                 if (!mbar_wait(acc_empty, (tc & 1u) ^ 1u, abort_flag)) {
                     *abort_flag = 1;
@@ -507,16 +540,21 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const int nk = min(4, k64_total - 4 * kt);
+                    const int nk = min(4, kmma_total - 4 * kt);
                     // descriptors advance 32 bytes (2 in the >>4 address field) per K step
                     const uint64_t ad = adesc0 + (uint64_t)s * (GM_STAGE_BYTES >> 4);
                     const uint64_t bd = bdesc0 + (uint64_t)s * (GM_STAGE_BYTES >> 4);
                     const uint32_t sf_col = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (j < nk)
-                            tc_mma(tmem, ad + 2 * j, bd + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
-                                   (kt > 0 || j > 0) ? 1u : 0u);
+                        if (j < nk) {
+                            if constexpr (FMT == 1)  // one scale column per operand half; byte j per MMA
+                                tc_mma_mx8(tmem, ad + 2 * j, bd + 2 * j, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29),
+                                           sf_col, sf_col + 16, (kt > 0 || j > 0) ? 1u : 0u);
+                            else
+                                tc_mma(tmem, ad + 2 * j, bd + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                                       (kt > 0 || j > 0) ? 1u : 0u);
+                        }
                     tc_commit(empty_bar(s));
                     issued_any = true;
                 }
@@ -561,12 +599,13 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
                     tc_fence_after();
                     for (int run = run0; run < run1; ++run) {
                         const uint32_t src = sbase + (uint32_t)s * GM_STAGE_BYTES +
-                                             (run == 0 ? GM_SFA_OFF : GM_SFB_OFF + 2048 * (run - 1));
+                                             (run == 0 ? GM_SFA_OFF : GM_SFB_OFF + (FMT ? 512 : 2048) * (run - 1));
                         const uint32_t dst = tmem + GM_SF_RING + (uint32_t)s * GM_SF_STAGE_COLS +
                                              (run == 0 ? 0u : 16u + 4u * (uint32_t)(run - 1));
                         const uint32_t step = run == 0 ? 4u : 8u;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) tc_cp_sf(dst + step * j, smem_desc(src + 512 * j, 16, 128, 0));
+                        for (int j = 0; j < (FMT ? 1 : 4); ++j)
+                            tc_cp_sf(dst + step * j, smem_desc(src + 512 * j, 16, 128, 0));
                     }
                     tc_commit(sf_bar(s));
                 }
@@ -732,12 +771,20 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(k_gemm_fp4<BSQ_EPI_SWIGLU_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(k_gemm_fp4<BSQ_EPI_F32, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)GmCfg<BSQ_EPI_F32>::SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(k_gemm_fp4<BSQ_EPI_BF16, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)GmCfg<BSQ_EPI_BF16>::SMEM_BYTES);
         return err;
     });
     if (aerr != cudaSuccess) return aerr;
     const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16;
-    const int64_t kb = a.K / 2;          // bytes per row of codes
-    const int64_t k64 = a.K / 64;        // SF chunks per row tile
+    const bool mx8 = a.fmt == 1;                 // MXFP8 operands (no SwiGLU epilogue)
+    if (mx8 && swiglu) return cudaErrorInvalidValue;
+    const int64_t kb = mx8 ? a.K : a.K / 2;      // bytes per row of codes
+    const int64_t k64 = mx8 ? a.K / 128 : a.K / 64;  // 512-byte SF chunks per row tile
     CUtensorMap tmA, tmB, tmSFB;
     {   // A: [m_capacity][K/2] bytes, box 128 x 128
         const cuuint64_t d[2] = {(cuuint64_t)kb, (cuuint64_t)a.m_capacity};
@@ -767,10 +814,11 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
         const cuuint32_t b[2] = {128u, 256u};
         if (!make_tmap(&tmB, a.b_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d, s, b, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        // B's SF as u64 [E*N/128 row tiles][k64 * 64]: one box = the 2 KB stage runs of two row tiles
+        // B's SF as u64 [E*N/128 row tiles][k64 * 64]: one box = the stage runs of two row tiles
+        // (2 KB each for NVFP4, 512 bytes for MXFP8)
         const cuuint64_t sd[2] = {(cuuint64_t)(k64 * 64), (cuuint64_t)(a.experts * a.N / 128)};
         const cuuint64_t ss[1] = {(cuuint64_t)(k64 * 512)};
-        const cuuint32_t sb[2] = {256u, 2u};
+        const cuuint32_t sb[2] = {mx8 ? 64u : 256u, 2u};
         if (!make_tmap(&tmSFB, a.b_sf, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
@@ -806,7 +854,14 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
     const int64_t max_tiles = ((a.m_capacity + 127) / 128) * p.n_tiles;
     const int64_t grid = std::min<int64_t>(max_tiles, a.sms);
     if (grid <= 0) return cudaSuccess;
-    if (swiglu)
+    if (mx8) {
+        if (a.epilogue == BSQ_EPI_BF16)
+            k_gemm_fp4<BSQ_EPI_BF16, 1><<<(unsigned)grid, GmCfg<BSQ_EPI_BF16>::THREADS, GmCfg<BSQ_EPI_BF16>::SMEM_BYTES,
+                                          st>>>(tmA, tmB, tmSFB, tmOut, p);
+        else
+            k_gemm_fp4<BSQ_EPI_F32, 1><<<(unsigned)grid, GmCfg<BSQ_EPI_F32>::THREADS, GmCfg<BSQ_EPI_F32>::SMEM_BYTES,
+                                         st>>>(tmA, tmB, tmSFB, tmOut, p);
+    } else if (swiglu)
         k_gemm_fp4<BSQ_EPI_SWIGLU_BF16><<<(unsigned)grid, GmCfg<BSQ_EPI_SWIGLU_BF16>::THREADS, GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES, st>>>(
             tmA, tmB, tmSFB, tmOut, p);
     else if (a.epilogue == BSQ_EPI_BF16)

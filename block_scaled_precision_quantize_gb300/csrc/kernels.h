@@ -52,6 +52,7 @@ struct GemmArgs {
     int64_t ldo;
     int32_t* dev_status;
     int sms;  // SMs of the current device (persistent grid size)
+    int fmt = 0;  // 0: NVFP4 operands, 1: MXFP8 operands
 };
 cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st);
 

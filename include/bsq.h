@@ -309,6 +309,32 @@ bsq_status grouped_expert_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_sf,
                                    uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * grouped_expert_gemm_mxfp8: the same grouped GEMM on MXFP8 operands
+ * (kind::mxf8f6f4 with one E8M0 scale per 32 elements), for the backward
+ * GEMMs of the MXFP8 recipe ("Miles Blackwell RL ...", "Il supporto Miles
+ * ...": the weight- and data-gradient GEMMs run in MXFP8 too; "LMSYS Drops
+ * Miles ...", "Recipe 1: End-to-end MXFP8"), fed by the row copies of
+ * quantize_mxfp8_rowcol and the MXFP8 targets of requant_transpose_sr:
+ *   y[m][n] = sum_k A[m][k] * B[e][n][k] * a_scale[m] * b_scale[e]
+ * with A[m][k] = E4M3(code) * 2^(E8M0(sf) - 127) (and B likewise); pass ones
+ * as a_scale / b_scale for plain MXFP8.
+ *   a_codes, a_sf   A, E4M3 [m_capacity][K], E8M0 SF swizzled (rows padded
+ *                   to 128)
+ *   offsets         as for grouped_expert_gemm_fp4
+ *   b_codes, b_sf   B, E4M3 [experts][N][K], SF swizzled over the experts*N
+ *                   stacked rows
+ *   epilogue        BSQ_EPI_F32 or BSQ_EPI_BF16 (out [m_capacity][ldo])
+ * K % 128 == 0; N % 128 == 0.
+ * ------------------------------------------------------------------------- */
+bsq_status grouped_expert_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_sf,
+                                     const float* a_scale, const int32_t* offsets,
+                                     int64_t experts, int64_t m_capacity, int64_t K, int64_t N,
+                                     const uint8_t* b_codes, const uint8_t* b_sf,
+                                     const float* b_scale, int32_t epilogue,
+                                     void* out, int64_t ldo,
+                                     uint32_t flags, int32_t* dev_status, bsq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * moe_expert_forward: routed-expert SwiGLU MLP with NVFP4 activations and
  * weights, one GPU:
  *   1. route: count rows per expert, pad each expert's segment to 128 rows,
