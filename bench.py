@@ -70,6 +70,8 @@ def peaks():
     # FP4 dense tensor peak = bf16 peak x the nominal FP4/BF16 ratio (13.5 / 2.25)
     p["fp4_tflops"] = p["bf16_tflops"] * 6.0
     p["fp4_tflops_sustained"] = p["bf16_tflops_sustained"] * 6.0
+    # FP8 dense tensor peak = bf16 peak x the nominal FP8/BF16 ratio (4.5 / 2.25)
+    p["fp8_tflops_sustained"] = p["bf16_tflops_sustained"] * 2.0
     return p
 
 
@@ -451,7 +453,8 @@ def run_ours(args, w, rank, world, local):
            "h2d_bytes_per_step": T * H * 2 + ids.nbytes + wts.nbytes, "d2h_bytes_per_step": T * H * 2,
            "copies": "double-buffered on two copy streams, overlapping the forwards"}
 
-    components = {} if args.no_components else quantizer_components(bsq, synth, dev, P)
+    components = {} if args.no_components else {**quantizer_components(bsq, synth, dev, P),
+                                                 **backward_gemm_components(bsq, dev, P)}
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -485,6 +488,49 @@ def time_rotating(launch, nsets, iters):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / iters
+
+
+def backward_gemm_components(bsq, dev, P):
+    """The MXFP8 grouped GEMM of the backward pass through the C ABI: the down
+    projection's data gradient on the Qwen3-shaped layer (dh = dout . W_d over
+    128 expert segments of 1024 / 1152 rows: M = 139264, K = H = 2048,
+    N = I = 768, bf16 out), random finite E4M3 codes and E8M0 scales around 1,
+    two input/output sets (1.4 GB) rotated."""
+    import torch
+    L = bsq.load()
+    st = torch.cuda.current_stream(dev).cuda_stream
+    E, K, N = 128, 2048, 768
+    counts = [1024 if e % 2 == 0 else 1152 for e in range(E)]
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device=dev)
+    M = int(sum(counts))
+    g = torch.Generator(device=dev).manual_seed(13)
+
+    def codes(*shape):
+        c = torch.randint(0, 0x7E, shape, dtype=torch.uint8, device=dev, generator=g)
+        return c | (torch.randint(0, 2, shape, dtype=torch.uint8, device=dev, generator=g) << 7)
+
+    def sfs(rows):
+        return torch.randint(120, 135, (bsq.sf_swizzled_bytes(rows, K // 32),), dtype=torch.uint8, device=dev,
+                             generator=g)
+
+    ones_m = torch.ones(M, dtype=torch.float32, device=dev)
+    ones_e = torch.ones(E, dtype=torch.float32, device=dev)
+    n = 2
+    sets = [(codes(M, K), sfs(M), codes(E, N, K), sfs(E * N), torch.empty(M, N, dtype=torch.bfloat16, device=dev))
+            for _ in range(n)]
+
+    def mm(i):
+        a, asf, b, bsf, out = sets[i % n]
+        L.grouped_expert_gemm_mxfp8(a.data_ptr(), asf.data_ptr(), ones_m.data_ptr(), offsets.data_ptr(), E, M, K, N,
+                                    b.data_ptr(), bsf.data_ptr(), ones_e.data_ptr(), bsq.EPI_BF16, out.data_ptr(), N,
+                                    bsq.SF_SWIZZLED, None, st)
+
+    us = time_rotating(mm, n, 10 * n) * 1e3
+    flop = 2.0 * M * N * K
+    del sets
+    return {"mxfp8_gemm_dgrad_qwen3": {"us": us, "tflop": flop / 1e12, "tflops": flop / (us * 1e-6) / 1e12,
+                                       "frac_of_fp8_peak": flop / (us * 1e-6) / 1e12 / P["fp8_tflops_sustained"],
+                                       "shape": "M=139264 (128 experts) K=2048 N=768, bf16 out", "sets": n}}
 
 
 def quantizer_components(bsq, synth, dev, P):
