@@ -107,3 +107,22 @@ def test_host_validation_of_dequantize_and_2d_without_a_gpu(lib):
     assert lib.quantize_nvfp4_2d(P(4100), 32, 256, d, d, d, d, d, 0, None, None) == 3  # x alignment
     assert lib.quantize_nvfp4_2d(d, 32, 256, d, d, P(4100), d, d, 0, None, None) == 3  # codes_t alignment
     assert lib.quantize_nvfp4_2d(d, 0, 256, d, d, d, d, d, 0, None, None) == 0         # empty: no-op
+
+
+def test_host_validation_of_rht_and_mxfp8_gemm_without_a_gpu(lib):
+    P = ctypes.c_void_p
+    d = P(4096)
+    # quantize_nvfp4_rht(x, rows, K, ldx, seed, codes, sf, scale, flags, status, stream)
+    assert lib.quantize_nvfp4_rht(d, 8, 256, 256, 7, d, d, d, 1 << 6, None, None) == 4  # flags
+    assert lib.quantize_nvfp4_rht(d, 8, 48, 48, 7, d, d, d, 0, None, None) == 2         # K % 32
+    assert lib.quantize_nvfp4_rht(d, 8, 256, 128, 7, d, d, d, 0, None, None) == 2       # ldx < K
+    assert lib.quantize_nvfp4_rht(None, 8, 256, 256, 7, d, d, d, 0, None, None) == 1    # null
+    assert lib.quantize_nvfp4_rht(P(4100), 8, 256, 256, 7, d, d, d, 0, None, None) == 3  # alignment
+    assert lib.quantize_nvfp4_rht(d, 0, 256, 256, 7, d, d, d, 0, None, None) == 0       # empty: no-op
+    # grouped_expert_gemm_mxfp8(a, asf, ascale, offsets, E, M, K, N, b, bsf, bscale, epi, out, ldo, flags, st, s)
+    assert lib.grouped_expert_gemm_mxfp8(d, d, d, d, 1, 128, 192, 128, d, d, d, 0, d, 128, 1, None, None) == 2  # K % 128
+    assert lib.grouped_expert_gemm_mxfp8(d, d, d, d, 1, 128, 256, 96, d, d, d, 0, d, 128, 1, None, None) == 2   # N % 128
+    assert lib.grouped_expert_gemm_mxfp8(d, d, d, d, 1, 128, 256, 128, d, d, d, 2, d, 128, 1, None, None) == 4  # no SwiGLU
+    assert lib.grouped_expert_gemm_mxfp8(d, d, d, d, 1, 128, 256, 128, d, d, d, 0, d, 64, 1, None, None) == 2   # ldo < N
+    assert lib.grouped_expert_gemm_mxfp8(d, d, None, d, 1, 128, 256, 128, d, d, d, 0, d, 128, 1, None, None) == 1
+    assert lib.grouped_expert_gemm_mxfp8(d, d, d, d, 1, 0, 256, 128, d, d, d, 0, d, 128, 1, None, None) == 0     # empty
