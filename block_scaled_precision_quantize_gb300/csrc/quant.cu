@@ -1025,22 +1025,28 @@ cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, cons
 // outliers over their group before block quantization).  Per group of 32
 // consecutive elements, y = H32 (s . x) with the Sylvester matrix unnormalized,
 // in binary32 by the butterfly h = 1, 2, 4, 8, 16; s = the 32 bits of word 0
-// of Philox4x32-10(seed, (0, 0, 2, 0)) (bit j set: s_j = -1).  One warp per
-// row; lane l holds the 16-element blocks l, l + 32, ... of a chunk of 128
-// blocks, so a block's group partner (block b ^ 1) sits in lane l ^ 1 at the
-// same register slot: stages 1-8 run in registers, stage 16 is one shuffle.
-// Rows of up to 128 blocks are quantized from registers; longer rows take two
-// passes over their chunks (the transformed row's maximum, then the encode).
+// of Philox4x32-10(seed, (0, 0, 2, 0)) (bit j set: s_j = -1).  Two warps per
+// row: of each chunk of 128 blocks (2048 elements), warp h takes blocks
+// 64 h + lane + 32 i (i < 2), so a block's group partner (block b ^ 1) sits in
+// lane l ^ 1 of the same warp at the same register slot: stages 1-8 run in
+// registers, stage 16 is one shuffle.  The row maximum is folded over the two
+// warps in shared memory.  Rows of up to 128 blocks are quantized from
+// registers (32 values a lane: ~64 registers, 32 warps an SM); longer rows
+// take two passes over their chunks (the transformed row's maximum, then the
+// encode).  One warp per whole row held 64 values a lane at 128 registers
+// and 16 warps an SM, and took 37.5 us on 16384 x 2048; this form takes
+// 35.2 us with four CTAs an SM (64 registers, a small spill) and 35.9 us with
+// three, so occupancy is not what bounds it.
 namespace {
 
-BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int c0, int lane, uint32_t signs,
-                           float (&v)[4][16], int nb)
+BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int b0, int lane, uint32_t signs,
+                           float (&v)[2][16])
 {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int b = c0 + lane + 32 * i;
+    for (int i = 0; i < 2; ++i) {
+        const int b = b0 + lane + 32 * i;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
-        if (i < nb && b < nblk) {
+        if (b < nblk) {
             a = ldg_stream(xr + 16 * b);
             c = ldg_stream(xr + 16 * b + 8);
         }
@@ -1069,45 +1075,54 @@ BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int c0, in
     }
 }
 
-template <int NB, bool SWZ>
-__global__ void __launch_bounds__(256) k_nvfp4_rht(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ldx,
+template <bool SWZ>
+__global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ldx,
                                                    uint64_t seed, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                    float* __restrict__ row_scale)
 {
     pdl_enter();
-    const int lane = threadIdx.x & 31;
+    __shared__ float s_max[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, half = warp & 1;
     const int nblk = (int)(K >> 4);
     const int ncol_pad = SWZ ? ((nblk + 3) & ~3) : nblk;
+    const int64_t nct = (ncol_pad + 3) >> 2;
     const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const uint32_t signs = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32)).x;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows_iter; r += nwarps) {
-        if (r >= rows) {  // swizzle padding rows
-            for (int b = lane; b < ncol_pad; b += 32) sf[sf_swizzled(r, b, (ncol_pad + 3) >> 2)] = 0u;
-            continue;
-        }
+    // CTA-uniform loop over groups of 4 rows (the shared-memory fold synchronizes the CTA)
+    for (int64_t r0 = (int64_t)blockIdx.x * 4; r0 < rows_iter; r0 += (int64_t)gridDim.x * 4) {
+        const int64_t r = r0 + (warp >> 1);
+        const bool real = r < rows;
         const uint16_t* xr = x + r * ldx;
-        float v[4][16];
+        float v[2][16];
         float amax = 0.0f;
         for (int c0 = 0; c0 < nblk; c0 += 128) {  // one chunk for rows of up to 128 blocks
-            rht_blocks(xr, nblk, c0, lane, signs, v, NB);
+            if (real) rht_blocks(xr, nblk, c0 + 64 * half, lane, signs, v);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+                for (int j = 0; j < 16; ++j) amax = real ? fmaxf(amax, fabsf(v[i][j])) : 0.0f;
         }
         amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax)));  // non-negative: bit order
+        if (lane == 0) s_max[warp] = amax;
+        __syncthreads();
+        amax = fmaxf(s_max[warp & ~1], s_max[warp | 1]);
+        __syncthreads();
+        if (r >= rows_iter) continue;
+        if (!real) {  // swizzle padding rows: zero scale factors
+            for (int b = 32 * half + lane; b < ncol_pad; b += 64) sf[sf_swizzled(r, b, nct)] = 0u;
+            continue;
+        }
         const float t = __fdiv_rn(amax, kNvfp4ScaleDivisor);
-        if (lane == 0) row_scale[r] = t;
+        if (lane == 0 && half == 0) row_scale[r] = t;
         const float six_t = __fmul_rn(6.0f, t);
         uint2* crow = reinterpret_cast<uint2*>(codes + r * (K >> 1));
         for (int c0 = 0; c0 < nblk; c0 += 128) {
-            if (nblk > 128) rht_blocks(xr, nblk, c0, lane, signs, v, NB);  // second pass: transform again
+            if (nblk > 128) rht_blocks(xr, nblk, c0 + 64 * half, lane, signs, v);  // second pass: transform again
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int b = c0 + lane + 32 * i;
-                if (i >= NB || b >= nblk) {
-                    if (SWZ && i < NB && b < ncol_pad) sf[sf_swizzled(r, b, (ncol_pad + 3) >> 2)] = 0u;
+            for (int i = 0; i < 2; ++i) {
+                const int b = c0 + 64 * half + lane + 32 * i;
+                if (b >= nblk) {
+                    if (SWZ && b < ncol_pad) sf[sf_swizzled(r, b, nct)] = 0u;
                     continue;
                 }
                 uint2 c = make_uint2(0u, 0u);
@@ -1121,7 +1136,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_rht(const uint16_t* __restrict__ 
                     sfb = bs.sf;
                 }
                 crow[b] = c;
-                sf[SWZ ? sf_swizzled(r, b, (ncol_pad + 3) >> 2) : r * nblk + b] = (uint8_t)sfb;
+                sf[SWZ ? sf_swizzled(r, b, nct) : r * nblk + b] = (uint8_t)sfb;
             }
         }
     }
@@ -1132,17 +1147,12 @@ __global__ void __launch_bounds__(256) k_nvfp4_rht(const uint16_t* __restrict__ 
 void launch_nvfp4_rht(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, uint64_t seed, uint8_t* codes,
                       uint8_t* sf, float* row_scale, bool swz, int sms, cudaStream_t st)
 {
-    const int64_t nblk = K >> 4;
     const int64_t rows_iter = swz ? ((rows + 127) & ~(int64_t)127) : rows;
-    const dim3 grid((unsigned)grid_for(rows_iter, sms));
-    const int nb = nblk <= 32 ? 1 : nblk <= 64 ? 2 : 4;
-#define BSQ_RHT(N, S) launch_k(k_nvfp4_rht<N, S>, grid, dim3(256), true, st, x, rows, K, ldx, seed, codes, sf, row_scale)
-    if (swz) {
-        if (nb == 1) BSQ_RHT(1, true); else if (nb == 2) BSQ_RHT(2, true); else BSQ_RHT(4, true);
-    } else {
-        if (nb == 1) BSQ_RHT(1, false); else if (nb == 2) BSQ_RHT(2, false); else BSQ_RHT(4, false);
-    }
-#undef BSQ_RHT
+    const dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>((rows_iter + 3) / 4, (int64_t)sms * 8)));
+    if (swz)
+        launch_k(k_nvfp4_rht<true>, grid, dim3(256), true, st, x, rows, K, ldx, seed, codes, sf, row_scale);
+    else
+        launch_k(k_nvfp4_rht<false>, grid, dim3(256), true, st, x, rows, K, ldx, seed, codes, sf, row_scale);
 }
 
 // ---------------------------------------------------------------- 2-D NVFP4
