@@ -510,3 +510,70 @@ def test_rht_quantization_is_the_per_row_recipe_of_the_transform(O):
     c2, s2 = O.nvfp4_quantize_rows_given_t(y, t_ref)
     np.testing.assert_array_equal(c, c2)
     np.testing.assert_array_equal(s, s2)
+
+
+def _nearest_e2m1_code(v):
+    """Brute-force E2M1 encoder, independent of the oracle's table: the
+    nearest of the 8 magnitudes by exact fp64 distance, ties to the even code,
+    saturating at 6, the sign bit taken from the input (so -0.0 -> 0x8)."""
+    v = np.asarray(v, np.float32)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    a = np.abs(v.astype(np.float64))
+    dist = np.abs(a[..., None] - mags)
+    best = dist.min(axis=-1, keepdims=True)
+    ties = dist == best
+    # among the tied magnitudes prefer an even code index (0, 2, 4, 6)
+    even = ties & (np.arange(8) % 2 == 0)
+    idx = np.where(even.any(axis=-1), even.argmax(axis=-1), ties.argmax(axis=-1))
+    idx = np.where(a >= 6.0, 7, idx)
+    return (idx | (np.signbit(v).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def _e4m3_rne(v):
+    """binary32 -> E4M3 byte by torch's float8_e4m3fn conversion (round to
+    nearest even), independent of the oracle's encoder."""
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_block_scale_and_codes_at_general_t(O):
+    """Steps 3 and 4 of the per-token recipe at per-token scales t != 1, each
+    byte recomputed with encoders that share nothing with the oracle: the
+    block scale is E4M3(rn(amax_b / rn(6 t))) by torch's float8 conversion,
+    the code the nearest E2M1 of rn(x * rn(1 / d)) with d = rn(E4M3(sf) * t),
+    by brute force ("End-to-End 4-Bit Training", section "先说为什么难": 16
+    E2M1 values share an E4M3 scale, and a second FP32 scale per token)."""
+    x = np.concatenate([synth.normal_with_outliers(192, 512, seed=41),
+                        synth.rows_log_uniform_std(64, 512, seed=42, lo_exp=-20, hi_exp=20)])
+    codes, sf, t = O.nvfp4_quantize_rows(x)
+    assert np.any(t != np.float32(1.0))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float32)
+    rows, K = xf.shape
+    blocks = xf.reshape(rows, K // 16, 16)
+    amax_b = np.abs(blocks).max(axis=-1).astype(np.float32)
+    six_t = (np.float32(6.0) * t).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s_raw = np.where(six_t[:, None] > 0, amax_b / six_t[:, None], np.float32(0)).astype(np.float32)
+    assert np.array_equal(sf, _e4m3_rne(s_raw)), "block scale bytes"
+    d = (e4m3_val(sf).astype(np.float32) * t[:, None]).astype(np.float32)   # exact product, one rounding
+    with np.errstate(divide="ignore", over="ignore"):
+        enc = np.where(d > 0, np.float32(1.0) / d, np.float32(0)).astype(np.float32)
+    enc = np.where(np.isinf(enc), np.finfo(np.float32).max, enc).astype(np.float32)
+    y = (blocks * enc[..., None]).astype(np.float32)
+    want = _nearest_e2m1_code(y).reshape(rows, K)
+    assert np.array_equal(unpack(codes), want), "element codes"
+    # the check has power against a division in place of the reciprocal:
+    # x / d differs from rn(x * rn(1/d)) on enough of these elements to flip codes
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y_div = np.where(d[..., None] > 0, blocks / d[..., None], np.float32(0)).astype(np.float32)
+    assert not np.array_equal(_nearest_e2m1_code(y_div).reshape(rows, K), want)
+
+
+def test_block_scale_at_general_t_detects_an_extra_rounding(O):
+    """The same block-scale pin has power against rounding 6 t twice (or
+    dividing by 6 then by t): on these rows at least one scale byte differs."""
+    x = synth.normal_with_outliers(256, 512, seed=43)
+    _, sf, t = O.nvfp4_quantize_rows(x)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float32)
+    amax_b = np.abs(xf.reshape(256, 32, 16)).max(axis=-1).astype(np.float32)
+    two_step = ((amax_b / np.float32(6.0)).astype(np.float32) / t[:, None]).astype(np.float32)
+    assert not np.array_equal(sf, _e4m3_rne(two_step))
