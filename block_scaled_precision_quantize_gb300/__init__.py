@@ -22,7 +22,7 @@ __all__ = [
     "quantize_nvfp4_2d", "quantize_nvfp4_rht", "dequantize_nvfp4", "requant_transpose_sr",
     "grouped_expert_gemm_fp4", "grouped_expert_gemm_mxfp8", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
-    "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes",
+    "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes", "mma_ceiling",
     "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
 ]
 
@@ -77,6 +77,7 @@ _SIGS = {
     "bsq_format_probe": (ctypes.c_int, [_I32, _P, _P, _P, _I64, _P]),
     "bsq_philox_bits16": (ctypes.c_int, [_U64, _U32, _U64, _I64, _P, _P]),
     "bsq_set_stage_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _I32]),
+    "bsq_mma_ceiling": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.POINTER(_I32), _P, _P]),
 }
 
 _stage_array = None
@@ -401,6 +402,19 @@ def format_probe(kind, values, rbits=None):
     _check(load().bsq_format_probe(kind, _ptr(values), _ptr(rbits), _ptr(out), n, _stream(values.device)),
            "bsq_format_probe")
     return out
+
+
+def mma_ceiling(fmt, cta_group, iters, device="cuda", dev_status=None):
+    """Launch the MMA-ceiling kernel once (fmt 0 NVFP4 / 1 MXFP8, cta_group 1
+    or 2, `iters` MMAs per CTA) on the current stream.  Returns (ctas,
+    cycles): the CTAs launched and a device uint64 tensor of per-CTA cycle
+    counts (0 for the second CTA of a pair)."""
+    props = torch.cuda.get_device_properties(device)
+    cycles = torch.zeros(props.multi_processor_count, dtype=torch.int64, device=device)
+    ctas = _I32(0)
+    _check(load().bsq_mma_ceiling(int(fmt), int(cta_group), int(iters), _ptr(cycles), ctypes.byref(ctas),
+                                  _ptr(dev_status), _stream(cycles.device)), "bsq_mma_ceiling")
+    return ctas.value, cycles
 
 
 def philox_bits16(seed, stream_id, idx0, n, device="cuda"):

@@ -18,8 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libbsq.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_fp4.cu", "moe.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+SOURCES = ["api.cu", "quant.cu", "gemm_fp4.cu", "moe.cu", "ceiling.cu"]
+HEADERS = ["common.cuh", "kernels.h", "tc_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",
               "-prec-sqrt=true", "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
@@ -70,6 +70,34 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+STALL_LIB = os.path.join(BUILD, "libbsq_gemm_stall.so")
+
+
+def build_gemm_stall_test_lib() -> str:
+    """A test-only copy of the library whose grouped GEMM is compiled with
+    BSQ_GEMM_STALL_HOOK: its producer never issues a copy and its waits give
+    up after a few thousand polls, so a test can watch the bounded-wait
+    timeout path end with BSQ_DEV_TIMEOUT while nothing asynchronous is in
+    flight.  The other objects are the product build's."""
+    build()
+    src = os.path.join(CSRC, "gemm_fp4.cu")
+    if os.path.exists(STALL_LIB) and os.path.getmtime(STALL_LIB) >= os.path.getmtime(LIB):
+        return STALL_LIB
+    cc = nvcc()
+    obj = os.path.join(BUILD, "gemm_fp4_stall.o")
+    r = subprocess.run([cc, *ARCH, *NVCC_FLAGS, "-DBSQ_GEMM_STALL_HOOK", "-c", src, "-o", obj],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for the stall-hook GEMM:\n{r.stdout}\n{r.stderr}")
+    objs = [os.path.join(BUILD, os.path.splitext(x)[0] + ".o") for x in SOURCES if x != "gemm_fp4.cu"] + [obj]
+    tmp = STALL_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, STALL_LIB)
+    return STALL_LIB
 
 
 if __name__ == "__main__":

@@ -498,6 +498,23 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
     return launched();
 }
 
+bsq_status bsq_mma_ceiling(int32_t fmt, int32_t cta_group, int32_t iters, uint64_t* cycles, int32_t* ctas,
+                           int32_t* dev_status, bsq_stream_t stream)
+{
+    if ((fmt != 0 && fmt != 1) || (cta_group != 1 && cta_group != 2)) return BSQ_ERR_FLAGS;
+    if (iters <= 0 || iters > 65536) return BSQ_ERR_SHAPE;
+    if (!cycles || !ctas) return BSQ_ERR_NULL;
+    int sms;
+    bsq_status st = current_device(&sms);
+    if (st != BSQ_OK) return st;
+    const int n = sms / cta_group * cta_group;
+    *ctas = n;
+    if (launch_mma_ceiling(fmt, cta_group, iters, reinterpret_cast<unsigned long long*>(cycles), dev_status, n,
+                           stream) != cudaSuccess)
+        return BSQ_ERR_CUDA;
+    return launched();
+}
+
 bsq_status bsq_sf_swizzle(const uint8_t* sf_linear, int64_t rows, int64_t cols, uint8_t* sf_swizzled,
                           bsq_stream_t stream)
 {

@@ -53,6 +53,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace bsq {
 
@@ -68,7 +69,16 @@ constexpr int GM_TMEM_COLS = 512;
 constexpr int GM_SF_RING = 256;                       // first SF column
 constexpr int GM_SF_STAGE_COLS = 48;
 constexpr int GM_MAX_SMEM_EXPERTS = 256;              // offsets cached in shared memory up to this E
+#ifdef BSQ_GEMM_STALL_HOOK
+// Test build only (never the product library): the producer issues no copies
+// and never arrives, and every wait gives up after a few thousand polls, so
+// each role takes its timeout path with nothing asynchronous in flight.
+constexpr uint32_t GM_SPIN_LIMIT = 1u << 12;
+constexpr bool GM_STALL = true;
+#else
 constexpr uint32_t GM_SPIN_LIMIT = 1u << 22;
+constexpr bool GM_STALL = false;
+#endif
 constexpr int GM_EPI_WARP_BYTES = 32 * 64;                     // 32 rows x 64 bytes, 64-byte swizzled
 
 // Per epilogue kind: the stage count, whether the epilogue stages its stores
@@ -92,43 +102,6 @@ struct GmCfg {
 static_assert(GM_SF_RING + GM_MAX_STAGES * GM_SF_STAGE_COLS <= GM_TMEM_COLS, "SF ring exceeds tensor memory");
 static_assert(GmCfg<BSQ_EPI_SWIGLU_BF16>::SMEM_BYTES + 2048 <= 232448, "stage ring exceeds shared memory");
 
-// Instruction descriptors, kind::mxf4nvf4: A and B are E2M1 (format 1),
-// K-major, no negation, N>>3 at bit 17, M = 128 (M>>4 at bit 24), scale type
-// UE4M3 (bit 23 = 0), scale-factor ids 0, dense, K = 64.
-__host__ __device__ constexpr uint32_t gm_idesc(uint32_t n) { return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24); }
-// kind::mxf8f6f4 with scale_vec::1X (the MXFP8 operands of the backward
-// GEMMs): A and B E4M3 (format 0), scale type UE8M0 (bit 23), M = 128,
-// K = 32.  Each tensor-memory scale column holds four E8M0 bytes of a row,
-// those of four consecutive 32-element blocks; the byte an MMA reads is its
-// scale-factor id (B's at bits 4-5, A's at bits 29-30).
-__host__ __device__ constexpr uint32_t gm_idesc_mx8(uint32_t n, uint32_t sf_id)
-{
-    return (sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) | (sf_id << 29);
-}
-
-// ------------------------------------------------------------------ PTX
-BSQ_DEVICE uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-BSQ_DEVICE void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-BSQ_DEVICE void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-BSQ_DEVICE bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // Bounded wait; gives up when the abort flag is raised or the spin limit hit.
 BSQ_DEVICE bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
 {
@@ -139,90 +112,6 @@ BSQ_DEVICE bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
     return false;
 }
 
-BSQ_DEVICE void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-BSQ_DEVICE void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-BSQ_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-BSQ_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-BSQ_DEVICE void tc_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor: start >> 4 (bits 0-13), leading byte
-// offset >> 4 (16-29), stride byte offset >> 4 (32-45), version 1 (46),
-// swizzle mode (61-63: 0 none, 2 = 128-byte).
-BSQ_DEVICE uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)swz << 61);
-}
-
-BSQ_DEVICE void tc_cp_sf(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-BSQ_DEVICE void tc_mma_mx8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                           uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
-            d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
-        : "memory");
-}
-
-BSQ_DEVICE void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                       uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
-            d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
-        : "memory");
-}
-
-// 32 consecutive accumulator columns of this warp's 32 lanes, without waiting.
-BSQ_DEVICE void tc_ld32_issue(uint32_t taddr, uint32_t r[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-// Wait for this thread's outstanding tcgen05.ld, then make every loaded
-// register depend on the wait so no use can be scheduled before it.
-template <int N>
-BSQ_DEVICE void tc_ld_wait(uint32_t (&r)[N])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
-}
-
 BSQ_DEVICE uint32_t pack_bf16x2(float lo, float hi)
 {
     const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
@@ -230,29 +119,6 @@ BSQ_DEVICE uint32_t pack_bf16x2(float lo, float hi)
     return l | (h << 16);
 }
 
-
-BSQ_DEVICE void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-BSQ_DEVICE void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
-BSQ_DEVICE void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-        "[%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-        : "memory");
-}
 
 // h = silu(g) * u with silu(g) = g / (1 + e^-g); approximate exponential and
 // division (relative error ~1e-6, far below the bf16 output rounding); the
@@ -434,7 +300,7 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmSFB)) : "memory");
             uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag && !GM_STALL; tile += gridDim.x) {
                 const TileInfo t = tile_info(tile);
                 const uint8_t* sfa_src = p.a_sf + ((size_t)(t.m0 >> 7) * sf_chunks) * 512;
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
@@ -492,7 +358,7 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
                 // loads from this thread are slow while the copies stream in)
                 const int nt = tile % p.n_tiles;
                 const uint32_t n_w = (swiglu || nt * 256 + 128 < p.N) ? 256u : 128u;
-                const uint32_t idesc = FMT ? gm_idesc_mx8(n_w, 0u) : gm_idesc(n_w);
+                const uint32_t idesc = FMT ? idesc_mxf8(n_w, 0u) : idesc_nvf4(n_w);
                 // the epilogue has taken the previous accumulator out of tensor memory
                 if (!mbar_wait(acc_empty, (tc & 1u) ^ 1u, abort_flag)) {
                     *abort_flag = 1;
@@ -521,10 +387,10 @@ __global__ void __launch_bounds__(GmCfg<EPI>::THREADS, 1)
                     for (int j = 0; j < 4; ++j)
                         if (j < nk) {
                             if constexpr (FMT == 1)  // one scale column per operand half; byte j per MMA
-                                tc_mma_mx8(tmem, ad + 2 * j, bd + 2 * j, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29),
+                                tc_mma_bs<1>(tmem, ad + 2 * j, bd + 2 * j, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29),
                                            sf_col, sf_col + 16, (kt > 0 || j > 0) ? 1u : 0u);
                             else
-                                tc_mma(tmem, ad + 2 * j, bd + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                                tc_mma_bs<0>(tmem, ad + 2 * j, bd + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
                                        (kt > 0 || j > 0) ? 1u : 0u);
                         }
                     tc_commit(empty_bar(s));

@@ -55,6 +55,8 @@ struct GemmArgs {
     int fmt = 0;  // 0: NVFP4 operands, 1: MXFP8 operands
 };
 cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_mma_ceiling(int fmt, int cta_group, int iters, unsigned long long* cycles, int32_t* dev_status,
+                               int ctas, cudaStream_t st);
 
 void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_t* hist, int32_t* counts,
                   int32_t* offsets, int32_t* slot_of, int32_t* row_src, int64_t capacity, int32_t* dev_status,

@@ -267,7 +267,9 @@ bsq_status requant_transpose_sr(const uint8_t* codes, const uint8_t* sf, const f
  *     anything is enqueued.
  *   - The first call on each device looks up the array's device address
  *     (with that device current); make that first call before capturing the
- *     stream into a graph.
+ *     stream into a graph.  The address is kept for the life of the process,
+ *     so the function is not supported after cudaDeviceReset (which unloads
+ *     the library's device code) in the same process.
  *   - Every call on a device uses the same array and clears the part it
  *     needs first; calls whose GPU work overlaps (other streams, other host
  *     threads on the same device) race on it and must be serialized by the
@@ -415,6 +417,29 @@ bsq_status bsq_format_probe(int32_t kind, const float* in, const uint32_t* rbits
                             void* out, int64_t n, bsq_stream_t stream);
 bsq_status bsq_philox_bits16(uint64_t seed, uint32_t stream_id, uint64_t idx0, int64_t n,
                              uint16_t* out, bsq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * bsq_mma_ceiling: measures the tensor cores' block-scaled MMA ceiling, the
+ * denominator of the grouped GEMM's roofline fraction (the pages give only
+ * nominal FP4 throughputs: "End-to-End 4-Bit Training", section "先说为什么难").
+ * One CTA per SM issues `iters` back-to-back MMAs of the GEMM's own form from
+ * operands already in shared memory, scale factors already in tensor memory:
+ *   fmt        0 = NVFP4 (kind::mxf4nvf4 scale_vec::4X, 128 x 256 x 64 per CTA),
+ *              1 = MXFP8 (kind::mxf8f6f4 scale_vec::1X, 128 x 256 x 32 per CTA)
+ *   cta_group  1 = one CTA per MMA; 2 = clusters of two CTAs sharing one
+ *              256 x 256 MMA (cta_group::2)
+ *   iters      MMAs per CTA, 1..65536
+ *   cycles     device uint64 [number of SMs]: for each issuing CTA the
+ *              clock64 cycles from its first issue to the completion of its
+ *              last MMA; 0 for the second CTA of a pair
+ *   ctas       host out: the number of CTAs launched (the SMs, rounded down
+ *              to a multiple of cta_group)
+ * The caller times the launch (CUDA events) for the FLOP rate:
+ * ctas * iters * 2 * 128 * 256 * K FLOPs.  A wait that runs out is reported
+ * in dev_status as BSQ_DEV_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+bsq_status bsq_mma_ceiling(int32_t fmt, int32_t cta_group, int32_t iters, uint64_t* cycles, int32_t* ctas,
+                           int32_t* dev_status, bsq_stream_t stream);
 
 #ifdef __cplusplus
 }

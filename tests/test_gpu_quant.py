@@ -181,6 +181,7 @@ def test_requant_full_size(gpu, O, shape):
                                    seed=7, swizzled=True)
     nc, ns, nt, mc, ms = O.requant_transpose(codes, sf, t, sr=True, seed=7)
     _check(to_np(out["nv_codes"]), nc, "nvfp4 codes")
+    _check(to_np(out["nv_sf"]), O.sf_to_swizzled(ns), "nvfp4 sf")
     _check(to_np(out["nv_scale"]), nt, "nvfp4 scale")
     _check(to_np(out["mx_codes"]), mc, "mxfp8 codes")
     _check(to_np(out["mx_sf"]), O.sf_to_swizzled(ms), "mxfp8 sf")
