@@ -30,11 +30,15 @@ BSQ_DEVICE void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// Arrive on a barrier of any CTA of the cluster (a shared::cluster address),
-// releasing this thread's earlier writes at cluster scope.
+// Arrive on a barrier of any CTA of the cluster (a shared::cluster address)
+// with the default semantics (release at CTA scope).  Release at cluster scope
+// would first wait for every earlier global store of the thread to become
+// visible to the cluster, which costs the epilogue thousands of cycles per
+// tile; the tensor-memory hand-off it signals is ordered by the tcgen05
+// fences around it instead.
 BSQ_DEVICE void mbar_arrive_cluster(uint32_t cluster_bar)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 // Expect-tx on a barrier of any CTA of the cluster, counting one arrival.
 BSQ_DEVICE void mbar_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes)
@@ -248,6 +252,46 @@ BSQ_DEVICE void tc_mma_bs(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t i
 #undef BSQ_MMA_ASM
 }
 
+// The same MMA with two barrier polls issued just before it in the same
+// instruction stream: the tensor core's queue holds about one MMA, so a
+// blocking barrier wait between MMAs leaves the tensor pipe idle for the
+// wait's latency (~150 cycles), while polls issued ahead of an MMA and
+// resolved after it cost nothing.  Returns bit 0 = phase `parity1` of `bar1`
+// complete, bit 1 = phase `parity2` of `bar2` complete (non-blocking tests).
+template <int FMT, int CG = 1>
+BSQ_DEVICE uint32_t tc_mma_bs_poll2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                    uint32_t sfb, uint32_t accumulate, uint32_t bar1, uint32_t parity1, uint32_t bar2,
+                                    uint32_t parity2)
+{
+    uint32_t r;
+#define BSQ_MMA_POLL_ASM(CGS, KIND)                                                                            \
+    asm volatile("{\n\t.reg .pred p, q1, q2;\n\t.reg .b32 t1, t2;\n\t"                                         \
+                 "mbarrier.test_wait.parity.shared::cta.b64 q1, [%8], %9;\n\t"                                \
+                 "mbarrier.test_wait.parity.shared::cta.b64 q2, [%10], %11;\n\t"                              \
+                 "setp.ne.b32 p, %5, 0;\n\t"                                                                  \
+                 "tcgen05.mma.cta_group::" CGS "." KIND " [%1], %2, %3, %4, [%6], [%7], p;\n\t"                  \
+                 "selp.u32 t1, 1, 0, q1;\n\t"                                                                 \
+                 "selp.u32 t2, 2, 0, q2;\n\t"                                                                 \
+                 "or.b32 %0, t1, t2;\n\t}"                                                                    \
+                 : "=r"(r)                                                                                     \
+                 : "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb), "r"(bar1),  \
+                   "r"(parity1), "r"(bar2), "r"(parity2)                                                        \
+                 : "memory")
+    if constexpr (FMT == 0) {
+        if constexpr (CG == 2)
+            BSQ_MMA_POLL_ASM("2", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+        else
+            BSQ_MMA_POLL_ASM("1", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+    } else {
+        if constexpr (CG == 2)
+            BSQ_MMA_POLL_ASM("2", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+        else
+            BSQ_MMA_POLL_ASM("1", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+    }
+#undef BSQ_MMA_POLL_ASM
+    return r;
+}
+
 // Instruction descriptors.  kind::mxf4nvf4: A and B are E2M1 (format 1),
 // K-major, no negation, N >> 3 at bit 17, M >> 4 at bit 24 (128 for one CTA,
 // 256 for a pair), scale type UE4M3 (bit 23 = 0), scale-factor ids 0, dense,
@@ -298,5 +342,173 @@ BSQ_DEVICE void tc_st16(uint32_t taddr, const uint32_t* r)
         : "memory");
 }
 BSQ_DEVICE void tc_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- warp-issued forms
+// The tcgen05 and TMA instructions take their descriptors, addresses and
+// coordinates in warp-uniform registers.  Issued from a single active lane
+// (inside `if (lane == 0)`), every operand must first be made uniform, which
+// measured 2-3x slower MMA issue (280-420 cycles per 128-cycle MMA).  These
+// forms are called by all 32 lanes of a converged warp with identical
+// operands; one lane, chosen by elect.sync inside the instruction sequence,
+// executes the instruction.  elect.sync picks the lowest active lane, so
+// successive calls from a converged warp issue from the same lane, which
+// tcgen05.commit needs (it tracks the issuing thread's own earlier MMAs and
+// copies); the drains that guard the release of tensor memory do not rely on
+// that (tc_commit_all).
+#define BSQ_ELECT "{\n\t.reg .pred e_;\n\t.reg .b32 l_;\n\telect.sync l_|e_, 0xffffffff;\n\t"
+
+template <int FMT, int CG = 1>
+BSQ_DEVICE void tc_mma_bs_w(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                            uint32_t accumulate)
+{
+#define BSQ_MMA_W(CGS, KIND)                                                                                 \
+    asm volatile(BSQ_ELECT ".reg .pred p_;\n\tsetp.ne.b32 p_, %4, 0;\n\t"                                     \
+                 "@e_ tcgen05.mma.cta_group::" CGS "." KIND " [%0], %1, %2, %3, [%5], [%6], p_;\n\t}" ::"r"(d), \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)                       \
+                 : "memory")
+    if constexpr (FMT == 0) {
+        if constexpr (CG == 2)
+            BSQ_MMA_W("2", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+        else
+            BSQ_MMA_W("1", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+    } else {
+        if constexpr (CG == 2)
+            BSQ_MMA_W("2", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+        else
+            BSQ_MMA_W("1", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+    }
+#undef BSQ_MMA_W
+}
+
+// tc_mma_bs_w with two non-blocking barrier tests issued just before the MMA
+// (by every lane): the tensor core's queue holds about one MMA, so a blocking
+// barrier wait between MMAs leaves the pipe idle for the wait's latency, while
+// tests issued ahead of an MMA and resolved after it cost nothing.  Returns
+// bit 0 = phase `parity1` of `bar1` complete, bit 1 = phase `parity2` of `bar2`.
+template <int FMT, int CG = 1>
+BSQ_DEVICE uint32_t tc_mma_bs_poll2_w(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                      uint32_t sfb, uint32_t accumulate, uint32_t bar1, uint32_t parity1,
+                                      uint32_t bar2, uint32_t parity2)
+{
+    uint32_t r;
+#define BSQ_MMA_POLL_W(CGS, KIND)                                                                            \
+    asm volatile(BSQ_ELECT ".reg .pred p_, q1_, q2_;\n\t.reg .b32 t1_, t2_;\n\t"                              \
+                 "mbarrier.test_wait.parity.shared::cta.b64 q1_, [%8], %9;\n\t"                               \
+                 "mbarrier.test_wait.parity.shared::cta.b64 q2_, [%10], %11;\n\t"                             \
+                 "setp.ne.b32 p_, %5, 0;\n\t"                                                                 \
+                 "@e_ tcgen05.mma.cta_group::" CGS "." KIND " [%1], %2, %3, %4, [%6], [%7], p_;\n\t"             \
+                 "selp.u32 t1_, 1, 0, q1_;\n\t"                                                               \
+                 "selp.u32 t2_, 2, 0, q2_;\n\t"                                                               \
+                 "or.b32 %0, t1_, t2_;\n\t}"                                                                  \
+                 : "=r"(r)                                                                                    \
+                 : "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb), "r"(bar1), \
+                   "r"(parity1), "r"(bar2), "r"(parity2)                                                       \
+                 : "memory")
+    if constexpr (FMT == 0) {
+        if constexpr (CG == 2)
+            BSQ_MMA_POLL_W("2", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+        else
+            BSQ_MMA_POLL_W("1", "kind::mxf4nvf4.block_scale.scale_vec::4X");
+    } else {
+        if constexpr (CG == 2)
+            BSQ_MMA_POLL_W("2", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+        else
+            BSQ_MMA_POLL_W("1", "kind::mxf8f6f4.block_scale.scale_vec::1X");
+    }
+#undef BSQ_MMA_POLL_W
+    return r;
+}
+
+// tcgen05.commit from the elected lane (the one that issued the tracked MMAs
+// or copies); CG 2 multicasts to the barrier at this offset in the CTAs of
+// cta_mask.
+template <int CG = 1>
+BSQ_DEVICE void tc_commit_w(uint32_t bar, uint16_t cta_mask = 3)
+{
+    if constexpr (CG == 2)
+        asm volatile(BSQ_ELECT "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+                               "[%0], %1;\n\t}" ::"r"(bar),
+                     "h"(cta_mask)
+                     : "memory");
+    else
+        asm volatile(BSQ_ELECT "@e_ tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                         bar)
+                     : "memory");
+}
+// tcgen05.commit from every lane of the warp: the barrier (initialised with a
+// count of 32) completes once the asynchronous tcgen05 work of whichever lane
+// issued it has completed.  Guards the release of tensor memory.
+template <int CG = 1>
+BSQ_DEVICE void tc_commit_all(uint32_t bar, uint16_t cta_mask = 3)
+{
+    tc_commit<CG>(bar, cta_mask);
+}
+
+template <int CG = 1>
+BSQ_DEVICE void tc_cp_sf_w(uint32_t taddr, uint64_t sdesc)
+{
+    if constexpr (CG == 2)
+        asm volatile(BSQ_ELECT "@e_ tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                     : "memory");
+    else
+        asm volatile(BSQ_ELECT "@e_ tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                     : "memory");
+}
+
+BSQ_DEVICE void mbar_expect_tx_w(uint32_t bar, uint32_t bytes)
+{
+    asm volatile(BSQ_ELECT "@e_ mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+template <int CG = 1>
+BSQ_DEVICE void tma_load_2d_w(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar)
+{
+    if constexpr (CG == 2)
+        asm volatile(BSQ_ELECT "@e_ cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+                               "[%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(dst),
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+                     : "memory");
+    else
+        asm volatile(BSQ_ELECT "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+                               "{%2, %3}], [%4];\n\t}" ::"r"(dst),
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+                     : "memory");
+}
+template <int CG = 1>
+BSQ_DEVICE void tma_load_3d_w(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint32_t bar)
+{
+    if constexpr (CG == 2)
+        asm volatile(BSQ_ELECT "@e_ cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+                               "[%0], [%1, {%2, %3, %4}], [%5];\n\t}" ::"r"(dst),
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+                     : "memory");
+    else
+        asm volatile(BSQ_ELECT "@e_ cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+                               "{%2, %3, %4}], [%5];\n\t}" ::"r"(dst),
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+                     : "memory");
+}
+template <int CG = 1>
+BSQ_DEVICE void tma_load_4d_w(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w, uint32_t bar)
+{
+    if constexpr (CG == 2)
+        asm volatile(BSQ_ELECT "@e_ cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+                               "[%0], [%1, {%2, %3, %4, %5}], [%6];\n\t}" ::"r"(dst),
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+                     : "memory");
+    else
+        asm volatile(BSQ_ELECT "@e_ cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+                               "{%2, %3, %4, %5}], [%6];\n\t}" ::"r"(dst),
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+                     : "memory");
+}
+BSQ_DEVICE void bulk_load_w(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(BSQ_ELECT "@e_ cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 
 }  // namespace bsq
