@@ -510,6 +510,19 @@ def run_ours(args, w, rank, world, local):
     names = ["route", "quantize_scatter", "gemm1_swiglu", "quantize_h", "gemm2", "combine"]
     stage_ms = {n: statistics.mean(stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for i in range(Ks))
                 for s, n in enumerate(names)}
+    # the same step with h quantized inside GEMM1's epilogue (moe_expert_forward
+    # with BSQ_MOE_FUSED_H: bit-identical results), timed for comparison
+    fe0, fe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        bsq.moe_expert_forward(x, ids_d, wts_d, wgu, wd, I, four_six=four_six, workspace=ws, y=y, dev_status=status,
+                               fused_h=True)
+    fe0.record()
+    for _ in range(Ks):
+        bsq.moe_expert_forward(x, ids_d, wts_d, wgu, wd, I, four_six=four_six, workspace=ws, y=y, dev_status=status,
+                               fused_h=True)
+    fe1.record()
+    torch.cuda.synchronize()
+    fused_h_ms = fe0.elapsed_time(fe1) / Ks
     f1, f2 = gemm_flops(w)
     flops = f1 + f2
     value = flops * world / (ms_step * 1e-3) / 1e12
@@ -628,6 +641,7 @@ def run_ours(args, w, rank, world, local):
                        "l2": "working set ~1 GB > 129 MB L2; no flush between steps; components rotate input sets > 2x L2",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "mma_ceiling": ceiling, "stages": stages, "components": components, "e2e": e2e,
+            "step_with_h_quantized_in_gemm1_ms": fused_h_ms,
             "gpu_launches": KERNELS_PER_STEP * K, "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x_bits, ids)

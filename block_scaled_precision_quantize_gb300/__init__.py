@@ -23,12 +23,14 @@ __all__ = [
     "grouped_expert_gemm_fp4", "grouped_expert_gemm_mxfp8", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
     "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes", "mma_ceiling",
-    "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
+    "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "MOE_FUSED_H", "MOE_KEEP_H", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
 ]
 
 SF_SWIZZLED = 1 << 0
 FOUR_SIX = 1 << 1
 STOCHASTIC = 1 << 2
+MOE_FUSED_H = 1 << 3
+MOE_KEEP_H = 1 << 4
 EPI_F32, EPI_BF16, EPI_SWIGLU_BF16 = 0, 1, 2
 DEV_OK, DEV_TIMEOUT, DEV_BAD_OFFSETS, DEV_BAD_EXPERT = 0, 1, 2, 3
 
@@ -49,7 +51,7 @@ class BsqError(RuntimeError):
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "offsets", "counts", "slot_of", "row_src", "xq_codes", "xq_sf", "xq_scale", "h",
-        "hq_codes", "hq_sf", "hq_scale", "out", "scan", "total")] + [("capacity", ctypes.c_int64)]
+        "hq_codes", "hq_sf", "hq_scale", "out", "scan", "h_scratch", "total")] + [("capacity", ctypes.c_int64)]
 
 
 _SIGS = {
@@ -354,12 +356,13 @@ def moe_workspace_size(T, H, I, E, topk) -> int:
 
 
 def moe_expert_forward(x, topk_ids, topk_weights, wgu, wd, I, four_six=False, workspace=None, y=None,
-                       dev_status=None):
+                       dev_status=None, fused_h=False, keep_h=False):
     """Routed SwiGLU experts with NVFP4 activations/weights. x bf16 [T, H];
     topk_ids int32 [T, k]; topk_weights f32 [T, k]; wgu = (codes [E, 2I, H/2],
     sf, scale [E]); wd = (codes [E, H, I/2], sf, scale [E]). Returns y bf16
     [T, H]; pass `workspace` (uint8, moe_workspace_size bytes) to keep the
-    intermediates."""
+    intermediates.  fused_h=True quantizes h inside GEMM1's epilogue (same
+    results); with it, keep_h=True also keeps the bf16 h in the workspace."""
     _cuda(x, "x")
     T, H = x.shape
     k = topk_ids.shape[1]
@@ -372,7 +375,9 @@ def moe_expert_forward(x, topk_ids, topk_weights, wgu, wd, I, four_six=False, wo
     _check(load().moe_expert_forward(_ptr(x), T, H, I, E, k, _ptr(topk_ids), _ptr(topk_weights),
                                      _ptr(wgu[0]), _ptr(wgu[1]), _ptr(wgu[2]), _ptr(wd[0]), _ptr(wd[1]),
                                      _ptr(wd[2]), _ptr(y), _ptr(workspace), workspace.numel(),
-                                     FOUR_SIX if four_six else 0, _ptr(dev_status), _stream(dev)),
+                                     (FOUR_SIX if four_six else 0) | (MOE_FUSED_H if fused_h else 0) |
+                                     (MOE_KEEP_H if keep_h else 0),
+                                     _ptr(dev_status), _stream(dev)),
            "moe_expert_forward")
     return y
 

@@ -405,6 +405,7 @@ bsq_status bsq_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, 
     L->hq_scale = take((size_t)cap * 4);
     L->out = take((size_t)cap * H * 2);
     L->scan = take(((size_t)std::max<int64_t>(nchunks, 1) * E + 1) * 4);  // histograms + ticket
+    L->h_scratch = take((size_t)2 * BSQ_MOE_MAX_CTAS * 128 * I * 2);  // two units per CTA
     L->total = o;
     return BSQ_OK;
 }
@@ -421,7 +422,7 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
                               const uint8_t* wd_sf, const float* wd_scale, void* y, void* workspace,
                               size_t workspace_bytes, uint32_t flags, int32_t* dev_status, bsq_stream_t stream)
 {
-    if (flags & ~BSQ_FOUR_SIX) return BSQ_ERR_FLAGS;
+    if (flags & ~(BSQ_FOUR_SIX | BSQ_MOE_FUSED_H | BSQ_MOE_KEEP_H)) return BSQ_ERR_FLAGS;
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0 || topk > 32 || E > 4096) return BSQ_ERR_SHAPE;
     if (H % 128 != 0 || H > 8192 || I % 128 != 0 || I > 8192) return BSQ_ERR_SHAPE;
     if (T * topk > ((int64_t)1 << 30)) return BSQ_ERR_SHAPE;
@@ -438,6 +439,8 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
     int sms;
     st = current_device(&sms);
     if (st != BSQ_OK) return st;
+    if ((flags & BSQ_MOE_FUSED_H) && gemm_fp4_ctas(E, L.capacity, (2 * I) / 256, sms) > BSQ_MOE_MAX_CTAS)
+        return BSQ_ERR_UNSUPPORTED;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
     auto F32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
@@ -465,19 +468,36 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
     g1.b_codes = wgu_codes;
     g1.b_sf = wgu_sf;
     g1.b_scale = wgu_scale;
-    g1.epilogue = BSQ_EPI_SWIGLU_BF16;
     g1.out = ws + L.h;
     g1.ldo = I;
     g1.dev_status = dev_status;
     g1.sms = sms;
-    if (launch_gemm_fp4(g1, stream) != cudaSuccess) return BSQ_ERR_CUDA;
-    stage_mark(3, stream);
-
-    launch_nvfp4_rows(reinterpret_cast<const uint16_t*>(ws + L.h), cap, I, I, ws + L.hq_codes, ws + L.hq_sf,
-                      F32(L.hq_scale), nullptr, 1, f46, true, sms, false, stream);
-    stage_mark(4, stream);
+    if (flags & BSQ_MOE_FUSED_H) {
+        // SwiGLU with the per-token NVFP4 quantization of h fused in
+        g1.epilogue = f46 ? GM_EPI_SWIGLU_Q46 : GM_EPI_SWIGLU_Q;
+        g1.q_codes = ws + L.hq_codes;
+        g1.q_sf = ws + L.hq_sf;
+        g1.q_scale = F32(L.hq_scale);
+        g1.h_scratch = reinterpret_cast<uint16_t*>(ws + L.h_scratch);
+        g1.keep_h = (flags & BSQ_MOE_KEEP_H) != 0;
+        if (launch_gemm_fp4(g1, stream) != cudaSuccess) return BSQ_ERR_CUDA;
+        stage_mark(3, stream);
+        stage_mark(4, stream);
+    } else {
+        // SwiGLU -> bf16 h, then the per-token quantizer over h
+        g1.epilogue = BSQ_EPI_SWIGLU_BF16;
+        if (launch_gemm_fp4(g1, stream) != cudaSuccess) return BSQ_ERR_CUDA;
+        stage_mark(3, stream);
+        launch_nvfp4_rows(reinterpret_cast<const uint16_t*>(ws + L.h), cap, I, I, ws + L.hq_codes, ws + L.hq_sf,
+                          F32(L.hq_scale), nullptr, 1, f46, true, sms, false, stream);
+        stage_mark(4, stream);
+    }
 
     GemmArgs g2 = g1;
+    g2.q_codes = g2.q_sf = nullptr;
+    g2.q_scale = nullptr;
+    g2.h_scratch = nullptr;
+    g2.keep_h = false;
     g2.a_codes = ws + L.hq_codes;
     g2.a_sf = ws + L.hq_sf;
     g2.a_scale = F32(L.hq_scale);

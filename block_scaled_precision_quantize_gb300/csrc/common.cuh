@@ -329,6 +329,62 @@ BSQ_DEVICE uint2 encode16(const float x[16], float enc)
 
 // MXFP8 shared exponent from the bit pattern of a block maximum (> 0):
 // X = clamp(floor(log2 amax) - 8, -127, 127); returns X.
+// ---------------------------------------------------------------- NVFP4 block
+// max |x| of 16 bf16 values (two 16-byte words) as a bf16 magnitude pattern
+BSQ_DEVICE uint32_t absmax16(const uint4& a, const uint4& b)
+{
+    uint32_t m = absmax_bf16x2(0u, a.x);
+    m = absmax_bf16x2(m, a.y);
+    m = absmax_bf16x2(m, a.z);
+    m = absmax_bf16x2(m, a.w);
+    m = absmax_bf16x2(m, b.x);
+    m = absmax_bf16x2(m, b.y);
+    m = absmax_bf16x2(m, b.z);
+    m = absmax_bf16x2(m, b.w);
+    return fold_halves(m);
+}
+
+BSQ_DEVICE void unpack16(const uint4& a, const uint4& b, float x[16])
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w[i]);
+        x[2 * i + 1] = bf16_hi(w[i]);
+    }
+}
+
+// One 16-element block of bf16 -> E2M1 codes (2 words) and the E4M3 block
+// scale byte, given the row (or tensor) scale t: the per-token recipe, with
+// the 4/6 choice of block scale when FOUR_SIX.  Shared by the quantizers and
+// the grouped GEMM's fused quantization of h.
+template <bool FOUR_SIX>
+BSQ_DEVICE void nvfp4_block(const uint4& a, const uint4& b, uint32_t amax16_bits, float t, float six_t,
+                            float four_t, uint2& codes, uint32_t& sf)
+{
+    if (t == 0.0f) {
+        codes = make_uint2(0u, 0u);
+        sf = 0u;
+        return;
+    }
+    float x[16];
+    unpack16(a, b, x);
+    const float ab = bf16mag_to_f32(amax16_bits);
+    const BlockScale s6 = nvfp4_block_scale(ab, six_t, t);
+    codes = encode16(x, s6.enc);
+    sf = s6.sf;
+    if (FOUR_SIX) {
+        const BlockScale s4 = nvfp4_block_scale(ab, four_t, t);
+        const uint2 c4 = encode16(x, s4.enc);
+        const float e6 = block_sse(x, codes.x, codes.y, s6.d);
+        const float e4 = block_sse(x, c4.x, c4.y, s4.d);
+        if (e4 < e6) {
+            codes = c4;
+            sf = s4.sf;
+        }
+    }
+}
+
 BSQ_DEVICE int mx_exponent(uint32_t amax_bits)
 {
     const int e = (int)(amax_bits >> 23);

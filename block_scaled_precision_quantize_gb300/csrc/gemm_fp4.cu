@@ -94,9 +94,14 @@ constexpr int GM_EPI_WARP_BYTES = 32 * 64;            // 32 rows x 64 bytes, 64-
 // a thread keeps 96 registers, which the SwiGLU epilogue needs to run without
 // spills.  One mover keeps the bf16 GEMM at 19 warps.  The pair form's 38 KB
 // stages fit five deep.
+template <int EPI>
+constexpr bool gm_swiglu = EPI == BSQ_EPI_SWIGLU_BF16 || EPI == GM_EPI_SWIGLU_Q || EPI == GM_EPI_SWIGLU_Q46;
+template <int EPI>
+constexpr bool gm_fused_q = EPI == GM_EPI_SWIGLU_Q || EPI == GM_EPI_SWIGLU_Q46;
+
 template <int EPI, int CG>
 struct GmCfg {
-    static constexpr int SF_WARPS = EPI == BSQ_EPI_SWIGLU_BF16 ? 2 : 1;
+    static constexpr int SF_WARPS = gm_swiglu<EPI> ? 2 : 1;
     static constexpr int THREADS = 32 * (2 + SF_WARPS + GM_EPI_WARPS);
     static constexpr bool STAGED = EPI == BSQ_EPI_BF16;
     static constexpr int B_BYTES = CG == 2 ? 16384 : 32768;
@@ -108,7 +113,8 @@ struct GmCfg {
 };
 static_assert(GM_SF_RING + GM_MAX_STAGES * GM_SF_STAGE_COLS <= GM_TMEM_COLS, "SF ring exceeds tensor memory");
 static_assert(GmCfg<BSQ_EPI_BF16, 2>::SMEM_BYTES + 2560 <= 232448, "stage ring exceeds shared memory");
-static_assert(GmCfg<BSQ_EPI_SWIGLU_BF16, 1>::SMEM_BYTES + 2560 <= 232448, "stage ring exceeds shared memory");
+static_assert(GmCfg<BSQ_EPI_SWIGLU_BF16, 1>::SMEM_BYTES + 3584 <= 232448, "stage ring exceeds shared memory");
+static_assert(GmCfg<GM_EPI_SWIGLU_Q, 2>::SMEM_BYTES + 3584 <= 232448, "stage ring exceeds shared memory");
 
 // Bounded wait; gives up when the abort flag is raised or the spin limit hit.
 // CLUSTER: acquire at cluster scope, for a barrier the other CTA of a pair
@@ -215,6 +221,52 @@ BSQ_DEVICE void st_row32(void* ptr, const uint32_t* w, bool vec32)
     }
 }
 
+// The per-token NVFP4 quantization of 128 rows of h (a GEMM1 unit) whose row
+// maxima, as bf16 magnitude bits, are already in smax (each is reset to 0 once
+// read): half-warp hw of 32 takes rows hw, hw + 32, ...; lane lr of it blocks
+// lr, lr + 16, ..., two at a time with their loads issued first.  The same
+// arithmetic as the per-token quantizer (nvfp4_block).
+template <bool FOUR_SIX>
+BSQ_DEVICE void gm_quantize_h_rows(uint32_t* smax, const uint8_t* hb, int64_t ldo, int nblk, int r0,
+                                                int m_capacity, uint8_t* q_codes, uint8_t* q_sf, float* q_scale,
+                                                int hw, int lr)
+{
+    for (int rr = hw; rr < 128; rr += 2 * GM_EPI_WARPS) {
+        const int grow = r0 + rr;
+        const uint32_t amax = smax[rr];
+        __syncwarp();
+        if (lr == 0) smax[rr] = 0u;  // the buffer's next unit comes after the next meeting
+        if (grow >= m_capacity) continue;
+        const float tq = __fdiv_rn(bf16mag_to_f32(amax), kNvfp4ScaleDivisor);
+        const float six_t = __fmul_rn(6.0f, tq), four_t = __fmul_rn(4.0f, tq);
+        const uint8_t* hr = hb + (size_t)rr * ldo * 2;
+        uint2* crow = reinterpret_cast<uint2*>(q_codes + (size_t)grow * (nblk * 8));
+        for (int b0 = lr; b0 < nblk; b0 += 32) {
+            uint4 va[2], vb[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int b = b0 + 16 * i;
+                if (b < nblk) {
+                    va[i] = __ldcg(reinterpret_cast<const uint4*>(hr + 32 * b));
+                    vb[i] = __ldcg(reinterpret_cast<const uint4*>(hr + 32 * b + 16));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int b = b0 + 16 * i;
+                if (b < nblk) {
+                    uint2 c;
+                    uint32_t sfv;
+                    nvfp4_block<FOUR_SIX>(va[i], vb[i], absmax16(va[i], vb[i]), tq, six_t, four_t, c, sfv);
+                    crow[b] = c;
+                    q_sf[sf_swizzled(grow, b, nblk >> 2)] = (uint8_t)sfv;
+                }
+            }
+        }
+        if (lr == 0) q_scale[grow] = tq;
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 struct GemmParams {
     const uint8_t* a_sf;
@@ -232,6 +284,14 @@ struct GemmParams {
     int32_t n_tiles;
     int32_t epilogue;
     bool out_vec32;  // output base and row pitch are 32-byte aligned
+    // fused quantization of h (GM_EPI_SWIGLU_Q*): NVFP4 h [m_capacity][N/4 bytes],
+    // its swizzled SF and per-row scale; the per-CTA bf16 scratch (128 x N/2),
+    // or h kept whole in `out` when keep_h
+    uint8_t* q_codes;
+    uint8_t* q_sf;
+    float* q_scale;
+    uint16_t* h_scratch;
+    bool keep_h;
 };
 
 struct TileInfo {
@@ -261,6 +321,9 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
     __shared__ int32_t s_poff[CG == 2 ? GM_MAX_SMEM_EXPERTS + 1 : 1];  // first pair tile of each expert
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort, s_bad;
+    // with the fused quantization of h: each row's running max |h| (bf16
+    // magnitude bits) over a unit's N tiles, double-buffered by unit
+    __shared__ uint32_t s_hmax[gm_fused_q<EPI> ? 2 : 1][128];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // the pair's first CTA issues the MMAs
@@ -294,6 +357,7 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
         mbar_init(drain_bar, 32);  // every lane of the issuing warp commits (tc_commit_all)
         for (int w = 0; w < SF_WARPS; ++w) mbar_init(sf_drain(w), 32);
         s_abort = 0;
+        for (int i = 0; i < (gm_fused_q<EPI> ? 256 : 128); ++i) (&s_hmax[0][0])[i] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -350,13 +414,25 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
         __syncthreads();
     }
 
-    constexpr bool swiglu = EPI == BSQ_EPI_SWIGLU_BF16;
+    constexpr bool swiglu = gm_swiglu<EPI>;
+    constexpr bool fused = gm_fused_q<EPI>;
     const int kmma_total = FMT ? (p.K >> 5) : (p.K >> 6);  // MMAs along K (64 or 32 elements each)
     const int kt_count = (kmma_total + 3) >> 2;
     const int sf_chunks = FMT ? (p.K >> 7) : (p.K >> 6);  // 512-byte scale chunks per 128-row tile
     const int m_units = s_bad ? 0 : (CG == 2 ? s_poff[E] : (off(E) + 127) >> 7);
     const int total_tiles = m_units * p.n_tiles;
     const int unit0 = (int)blockIdx.x / CG, unit_step = (int)gridDim.x / CG;
+    // The k-th tile of this CTA (pair): round-robin over the tiles, or, with the
+    // fused quantization of h, round-robin over the M units with each unit's N
+    // tiles in order, so that all of a row's h is produced on this CTA
+    auto tile_of = [&](int k) {
+        if constexpr (fused) {
+            const int u = unit0 + (k / p.n_tiles) * unit_step;
+            return u < m_units ? u * p.n_tiles + k % p.n_tiles : total_tiles;
+        } else {
+            return unit0 + k * unit_step;
+        }
+    };
 
     auto tile_info = [&](int tile) {
         TileInfo t;
@@ -394,7 +470,9 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
         }
         __syncwarp();
         uint32_t it = 0;
-        for (int tile = unit0; tile < total_tiles && !GM_STALL && !aborted_w(abort_flag); tile += unit_step) {
+        for (int k = 0; !GM_STALL && !aborted_w(abort_flag); ++k) {
+            const int tile = tile_of(k);
+            if (tile >= total_tiles) break;
             const TileInfo t = tile_info(tile);
             const int my_m0 = t.m0 + 128 * (int)rank;  // this CTA's 128 rows of A
             const uint8_t* sfa_src = p.a_sf + ((size_t)(my_m0 >> 7) * sf_chunks) * 512;
@@ -471,7 +549,9 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
             bool ready = false;  // stage `it` already seen complete (codes and scale factors)
             const uint64_t adesc0 = smem_desc(sbase + GM_A_OFF, 16, 1024, 2);
             const uint64_t bdesc0 = smem_desc(sbase + GM_B_OFF, 16, 1024, 2);
-            for (int tile = unit0; tile < total_tiles && !aborted_w(abort_flag); tile += unit_step, ++tc) {
+            for (int k = 0; !aborted_w(abort_flag); ++k, ++tc) {
+                const int tile = tile_of(k);
+                if (tile >= total_tiles) break;
                 // only the tile's width matters here (no expert lookup: shared-memory
                 // loads from this warp are slow while the copies stream in)
                 const int nt = tile % p.n_tiles;
@@ -558,7 +638,8 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
         const int w_sf = warp - 2;
         if (rank == 0) {
             uint32_t it = 0;
-            for (int tile = unit0; tile < total_tiles && !aborted_w(abort_flag); tile += unit_step) {
+            for (int k = 0; !aborted_w(abort_flag); ++k) {
+                if (tile_of(k) >= total_tiles) break;
                 bool stop = false;
                 for (int kt = 0; kt < kt_count; ++kt, ++it) {
                     const int s = (int)(it % STAGES);
@@ -606,7 +687,34 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
         uint8_t* stage_buf = smem + Cfg::EPI_OFF + (warp - 2 - SF_WARPS) * GM_EPI_WARP_BYTES;
         const uint32_t acc_empty_lead = lead(acc_empty);
         uint32_t tc = 0;
-        for (int tile = unit0; tile < total_tiles; tile += unit_step, ++tc) {
+        bool broke = false;
+        // fused quantization of h: the unit whose rows await quantization
+        bool pend_valid = false;
+        int pend_ub = 0, pend_row0 = 0;
+        // a unit's h rows: this CTA's scratch (by unit parity) or, with keep_h, h itself
+        auto unit_h = [&](int ub, int r0) {
+            return p.keep_h ? static_cast<uint8_t*>(p.out) + (size_t)r0 * p.ldo * 2
+                            : reinterpret_cast<uint8_t*>(p.h_scratch) + ((size_t)blockIdx.x * 2 + ub) * 128 * p.ldo * 2;
+        };
+        // The per-token NVFP4 quantization of a finished unit's 128 rows of h:
+        // the 16 epilogue warps meet (every store of the unit's h is then
+        // visible to all of them), then quantize (gm_quantize_h_rows)
+        auto quantize_unit = [&](int ub, int r0) {
+            __syncwarp();
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * GM_EPI_WARPS) : "memory");
+            gm_quantize_h_rows<EPI == GM_EPI_SWIGLU_Q46>(s_hmax[ub], unit_h(ub, r0), p.ldo, p.N >> 5, r0, p.m_capacity,
+                                                         p.q_codes, p.q_sf, p.q_scale,
+                                                         2 * (warp - 2 - SF_WARPS) + (lane >> 4), lane & 15);
+        };
+        for (int k = 0;; ++k, ++tc) {
+            const int tile = tile_of(k);
+            if (tile >= total_tiles) {
+                // after the last tile: the fused quantization's last unit
+                if constexpr (fused) {
+                    if (pend_valid) quantize_unit(pend_ub, pend_row0);
+                }
+                break;
+            }
             const TileInfo t = tile_info(tile);
             const int row0 = t.m0 + 128 * (int)rank;  // this CTA's rows of the tile
             const int row = row0 + 32 * q + lane;
@@ -624,6 +732,7 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
                     *abort_flag = 1;
                     report(p.dev_status, BSQ_DEV_TIMEOUT);
                 }
+                broke = true;
                 break;
             }
             tc_fence_after();
@@ -678,21 +787,42 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
                 tc_ld_wait(r);
             }
             hand_back();
-            if (!active) continue;
+            if (active) {
             const float s = (row < p.m_capacity) ? __fmul_rn(__ldg(p.a_scale + row), __ldg(p.b_scale + t.e)) : 0.0f;
             if constexpr (swiglu) {
                 // 32 h values = 64 contiguous bytes of this thread's row, stored
                 // from registers as two 32-byte sectors (or four 16-byte pieces
                 // when the output is only 16-byte aligned)
-                if (row < p.m_capacity) {
-                    uint32_t w[16];
+                if constexpr (!fused) {
+                    if (row < p.m_capacity) {
+                        uint32_t w[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[2 * j]) * s, __uint_as_float(r[32 + 2 * j]) * s),
-                                           swiglu1(__uint_as_float(r[2 * j + 1]) * s, __uint_as_float(r[33 + 2 * j]) * s));
-                    uint8_t* d = static_cast<uint8_t*>(p.out) + ((size_t)row * p.ldo + t.nt * 128 + 32 * part) * 2;
-                    st_row32(d, w, p.out_vec32);
-                    st_row32(d + 32, w + 8, p.out_vec32);
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[2 * j]) * s, __uint_as_float(r[32 + 2 * j]) * s),
+                                               swiglu1(__uint_as_float(r[2 * j + 1]) * s, __uint_as_float(r[33 + 2 * j]) * s));
+                        uint8_t* d = static_cast<uint8_t*>(p.out) + ((size_t)row * p.ldo + t.nt * 128 + 32 * part) * 2;
+                        st_row32(d, w, p.out_vec32);
+                        st_row32(d + 32, w + 8, p.out_vec32);
+                    }
+                } else {
+                    // h of this CTA's 128 rows goes to its scratch (double-buffered by
+                    // unit; h kept whole in `out` for staged checks), and each row's
+                    // running max |h|, over the bf16 values the quantizer will read,
+                    // to shared memory
+                    if (row < p.m_capacity) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = pack_bf16x2(swiglu1(__uint_as_float(r[2 * j]) * s, __uint_as_float(r[32 + 2 * j]) * s),
+                                               swiglu1(__uint_as_float(r[2 * j + 1]) * s, __uint_as_float(r[33 + 2 * j]) * s));
+                        uint32_t m = 0;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) m = absmax_bf16x2(m, w[j]);
+                        atomicMax(&s_hmax[(k / p.n_tiles) & 1][32 * q + lane], fold_halves(m));
+                        uint8_t* d = unit_h((k / p.n_tiles) & 1, row0) + ((size_t)(32 * q + lane) * p.ldo + t.nt * 128 + 32 * part) * 2;
+                        st_row32(d, w, p.out_vec32);
+                        st_row32(d + 32, w + 8, p.out_vec32);
+                    }
                 }
             } else if (row < p.m_capacity) {
                 float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (size_t)row * p.ldo + t.nt * 256 +
@@ -702,7 +832,20 @@ __global__ void __launch_bounds__(GmCfg<EPI, CG>::THREADS, 1)
                     d[i] = make_float4(__uint_as_float(r[4 * i]) * s, __uint_as_float(r[4 * i + 1]) * s,
                                        __uint_as_float(r[4 * i + 2]) * s, __uint_as_float(r[4 * i + 3]) * s);
             }
+            }
+            if constexpr (fused) {
+                // A unit's rows are quantized during the next unit's first tile,
+                // after its accumulator went back, so the MMAs keep running
+                if (t.nt == 0 && pend_valid) quantize_unit(pend_ub, pend_row0);
+                if (t.nt == 0) pend_valid = false;
+                if (t.nt == p.n_tiles - 1) {
+                    pend_valid = active;
+                    pend_ub = (k / p.n_tiles) & 1;
+                    pend_row0 = row0;
+                }
+            }
         }
+        (void)broke;
         if constexpr (Cfg::STAGED) {
             if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             __syncwarp();
@@ -804,6 +947,9 @@ static cudaError_t launch_form(const GemmArgs& a, int64_t grid, const CUtensorMa
                    : launch_kernel<BSQ_EPI_F32, 1, CG>(grid, tmA, tmB, tmSFA, tmSFB, tmOut, p, st);
     if (a.epilogue == BSQ_EPI_SWIGLU_BF16)
         return launch_kernel<BSQ_EPI_SWIGLU_BF16, 0, CG>(grid, tmA, tmB, tmSFA, tmSFB, tmOut, p, st);
+    if (a.epilogue == GM_EPI_SWIGLU_Q) return launch_kernel<GM_EPI_SWIGLU_Q, 0, CG>(grid, tmA, tmB, tmSFA, tmSFB, tmOut, p, st);
+    if (a.epilogue == GM_EPI_SWIGLU_Q46)
+        return launch_kernel<GM_EPI_SWIGLU_Q46, 0, CG>(grid, tmA, tmB, tmSFA, tmSFB, tmOut, p, st);
     if (a.epilogue == BSQ_EPI_BF16) return launch_kernel<BSQ_EPI_BF16, 0, CG>(grid, tmA, tmB, tmSFA, tmSFB, tmOut, p, st);
     return launch_kernel<BSQ_EPI_F32, 0, CG>(grid, tmA, tmB, tmSFA, tmSFB, tmOut, p, st);
 }
@@ -814,9 +960,21 @@ static cudaError_t set_form_attrs()
     cudaError_t err = set_smem_attr<BSQ_EPI_F32, 0, CG>();
     if (err == cudaSuccess) err = set_smem_attr<BSQ_EPI_BF16, 0, CG>();
     if (err == cudaSuccess) err = set_smem_attr<BSQ_EPI_SWIGLU_BF16, 0, CG>();
+    if (err == cudaSuccess) err = set_smem_attr<GM_EPI_SWIGLU_Q, 0, CG>();
+    if (err == cudaSuccess) err = set_smem_attr<GM_EPI_SWIGLU_Q46, 0, CG>();
     if (err == cudaSuccess) err = set_smem_attr<BSQ_EPI_F32, 1, CG>();
     if (err == cudaSuccess) err = set_smem_attr<BSQ_EPI_BF16, 1, CG>();
     return err;
+}
+
+// The form and the CTAs a launch uses (the pair form keeps every expert's
+// first pair tile in shared memory).
+static int gemm_form(int64_t experts, int sms) { return experts <= GM_MAX_SMEM_EXPERTS && sms >= 2 ? 2 : 1; }
+int64_t gemm_fp4_ctas(int64_t experts, int64_t m_capacity, int64_t n_tiles, int sms)
+{
+    const int64_t max_units = ((m_capacity + 127) / 128) * n_tiles;
+    if (gemm_form(experts, sms) == 2) return 2 * std::min<int64_t>(max_units, sms / 2);
+    return std::min<int64_t>(max_units, sms);
 }
 
 cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
@@ -827,11 +985,12 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
         return err == cudaSuccess ? set_form_attrs<2>() : err;
     });
     if (aerr != cudaSuccess) return aerr;
-    const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16;
+    const bool fused = a.epilogue == GM_EPI_SWIGLU_Q || a.epilogue == GM_EPI_SWIGLU_Q46;
+    const bool swiglu = a.epilogue == BSQ_EPI_SWIGLU_BF16 || fused;
     const bool mx8 = a.fmt == 1;                 // MXFP8 operands (no SwiGLU epilogue)
+    if (fused && (!a.q_codes || !a.q_sf || !a.q_scale || (!a.keep_h && !a.h_scratch))) return cudaErrorInvalidValue;
     if (mx8 && swiglu) return cudaErrorInvalidValue;
-    // the pair form keeps every expert's first pair tile in shared memory
-    const int cg = a.experts <= GM_MAX_SMEM_EXPERTS && a.sms >= 2 ? 2 : 1;
+    const int cg = gemm_form(a.experts, a.sms);
     const int64_t kb = mx8 ? a.K : a.K / 2;      // bytes per row of codes
     const int64_t k64 = mx8 ? a.K / 128 : a.K / 64;  // 512-byte SF chunks per row tile
     const int64_t m_tiles = (a.m_capacity + 127) / 128;
@@ -916,7 +1075,13 @@ cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st)
     p.K = (int32_t)a.K;
     p.N = (int32_t)a.N;
     p.epilogue = a.epilogue;
-    p.out_vec32 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0) && ((a.ldo * 2) % 32 == 0);
+    p.out_vec32 = (reinterpret_cast<uintptr_t>(fused && !a.keep_h ? (const void*)a.h_scratch : a.out) % 32 == 0) &&
+                  ((a.ldo * 2) % 32 == 0);
+    p.q_codes = a.q_codes;
+    p.q_sf = a.q_sf;
+    p.q_scale = a.q_scale;
+    p.h_scratch = a.h_scratch;
+    p.keep_h = a.keep_h;
     p.n_tiles = swiglu ? (int32_t)(a.N / 256) : (int32_t)((a.N + 255) / 256);
     // persistent: at most one CTA per SM, never more CTAs (or pairs) than the largest
     // possible tile count (a pair tile covers at least one 128-row tile)

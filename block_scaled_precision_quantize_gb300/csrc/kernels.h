@@ -53,7 +53,22 @@ struct GemmArgs {
     int32_t* dev_status;
     int sms;  // SMs of the current device (persistent grid size)
     int fmt = 0;  // 0: NVFP4 operands, 1: MXFP8 operands
+    // the fused SwiGLU + NVFP4-of-h epilogue (GM_EPI_SWIGLU_Q / _Q46): the
+    // quantized h, a scratch of 128 rows x N/2 bf16 per CTA, and whether h is
+    // also kept in full in `out` (for staged checks) instead of the scratch
+    uint8_t* q_codes = nullptr;
+    uint8_t* q_sf = nullptr;
+    float* q_scale = nullptr;
+    uint16_t* h_scratch = nullptr;
+    bool keep_h = false;
 };
+// Internal epilogue kinds (not part of the C ABI): SwiGLU with the per-token
+// NVFP4 quantization of h fused in, without / with the 4/6 block-scale choice.
+constexpr int GM_EPI_SWIGLU_Q = 8;
+constexpr int GM_EPI_SWIGLU_Q46 = 9;
+// The CTAs the grouped GEMM launches for a problem on `sms` SMs (the fused
+// epilogue's scratch holds 128 rows of h per CTA).
+int64_t gemm_fp4_ctas(int64_t experts, int64_t m_capacity, int64_t n_tiles, int sms);
 cudaError_t launch_gemm_fp4(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_mma_ceiling(int fmt, int cta_group, int iters, unsigned long long* cycles, int32_t* dev_status,
                                int ctas, cudaStream_t st);

@@ -81,6 +81,8 @@ typedef enum {
 #define BSQ_SF_SWIZZLED (1u << 0)   /* scale factors in the tensor-core tile layout */
 #define BSQ_FOUR_SIX (1u << 1)      /* NVFP4 "4/6" block-scale choice (activations only) */
 #define BSQ_STOCHASTIC (1u << 2)    /* stochastic rounding of element codes (requant) */
+#define BSQ_MOE_FUSED_H (1u << 3)   /* moe_expert_forward: quantize h inside GEMM1's epilogue */
+#define BSQ_MOE_KEEP_H (1u << 4)    /* with BSQ_MOE_FUSED_H: also keep the bf16 SwiGLU output h */
 
 /* GEMM epilogues */
 #define BSQ_EPI_F32 0         /* out fp32 [M][N] = acc * a_scale[row] * b_scale[expert] */
@@ -344,7 +346,14 @@ bsq_status grouped_expert_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_sf
  *   2. per-token NVFP4 quantization of x into the routed slots;
  *   3. grouped GEMM with gate/up weights and the fused SwiGLU + FP32 rescale
  *      epilogue -> h (bf16);
- *   4. per-token NVFP4 quantization of h (4/6 with BSQ_FOUR_SIX);
+ *   4. per-token NVFP4 quantization of h (4/6 with BSQ_FOUR_SIX).  With
+ *      BSQ_MOE_FUSED_H, step 3's epilogue does it instead: once all of a
+ *      row's N tiles are done on the CTA it quantizes the row from the
+ *      CTA's scratch, so h never reaches memory ("LMSYS Drops Miles ...",
+ *      section "Results": the per-token scaling inside the GEMM).  Same
+ *      results bit for bit; on GB300 it measured slower (the quantization
+ *      then runs on the 16 epilogue warps, already GEMM1's bottleneck,
+ *      instead of the whole GPU);
  *   5. grouped GEMM with down weights, rescale -> per-slot outputs (bf16);
  *   6. combine: y[t] = sum_j w[t][j] * out[slot(t, j)], fp32, j ascending.
  *   x              bf16 [T][H]
@@ -355,8 +364,14 @@ bsq_status grouped_expert_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_sf
  *   y              out bf16 [T][H]
  *   workspace      device scratch, bsq_moe_workspace_size() bytes; its
  *                  sub-buffers (bsq_moe_layout) hold the intermediates
- * H % 256 == 0, I % 128 == 0, topk <= 32.
+ *   flags          BSQ_FOUR_SIX (the 4/6 choice on x and h); BSQ_MOE_FUSED_H
+ *                  (above), and with it BSQ_MOE_KEEP_H, which also keeps the
+ *                  whole bf16 h in the layout's h buffer (for checking the
+ *                  stages separately), otherwise untouched in that mode
+ * H % 256 == 0, I % 128 == 0, topk <= 32; BSQ_MOE_FUSED_H on a device with
+ * more than BSQ_MOE_MAX_CTAS SMs is refused (BSQ_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------- */
+#define BSQ_MOE_MAX_CTAS 256  /* GEMM1 CTAs the h scratch is sized for */
 typedef struct {
     size_t offsets;      /* int32 [E+1]   padded segment starts */
     size_t counts;       /* int32 [E]     routed rows per expert */
@@ -365,13 +380,17 @@ typedef struct {
     size_t xq_codes;     /* u8 [cap][H/2] */
     size_t xq_sf;        /* u8 swizzled, cap x H/16 */
     size_t xq_scale;     /* fp32 [cap] */
-    size_t h;            /* bf16 [cap][I] */
+    size_t h;            /* bf16 [cap][I] (with BSQ_MOE_FUSED_H, only with BSQ_MOE_KEEP_H) */
     size_t hq_codes;     /* u8 [cap][I/2] */
     size_t hq_sf;        /* u8 swizzled, cap x I/16 */
     size_t hq_scale;     /* fp32 [cap] */
     size_t out;          /* bf16 [cap][H] per-slot expert outputs */
     size_t scan;         /* int32 scratch for the routing scan: per-512-pair
                             chunk expert histograms and a counter */
+    size_t h_scratch;    /* bf16 [BSQ_MOE_MAX_CTAS][2][128][I]: with
+                            BSQ_MOE_FUSED_H, each GEMM1 CTA's rows of h (two
+                            units) between the SwiGLU and their quantization
+                            (stays in L2) */
     size_t total;        /* bytes */
     int64_t capacity;    /* cap: T*topk + E*127 rounded up to 128 */
 } bsq_moe_layout;

@@ -5,7 +5,10 @@ an NVFP4 code of h, so the forward is checked in stages: routing (exact),
 quantize-scatter of x (bit-exact), GEMM1 + SwiGLU (GEMM tolerance + bf16),
 quantization of the GPU's own h (bit-exact), GEMM2 from the GPU's own
 quantized h (GEMM tolerance + bf16), combine of the GPU's own expert outputs
-(fp32 accumulation + bf16 rounding)."""
+(fp32 accumulation + bf16 rounding).  With BSQ_MOE_FUSED_H GEMM1 quantizes h
+in its epilogue instead; separate tests show that this changes no result bit
+(with and without keeping h), and check those stages on the full-size
+layers."""
 import numpy as np
 import pytest
 import torch
@@ -297,3 +300,62 @@ def test_moe_staged_many_experts(gpu, O):
     CTA version's expert limit) and the GEMM's offsets read from global
     memory."""
     _staged(gpu, O, T=160, H=256, I=128, E=600, k=3, four_six=False, seed=8)
+
+
+@pytest.mark.parametrize("four_six", [False, True])
+def test_moe_fused_h_quantization_bit_identical(gpu, four_six):
+    """BSQ_MOE_FUSED_H: GEMM1 quantizes h from its per-CTA scratch rows (or
+    from the kept whole h with BSQ_MOE_KEEP_H).  The quantized h, the
+    per-slot outputs and y equal, bit for bit, those of the two-pass path
+    (GEMM1 -> bf16 h -> the per-token quantizer), which the staged tests
+    check against the oracle (ragged experts, two N tiles per unit)."""
+    T, H, I, E, k = 300, 512, 256, 9, 4
+    x = synth.normal((T, H), seed=21)
+    ids, wts = synth.topk_routing(T, E, k, seed=21)
+    wgu = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, 2 * I, H), seed=22, std=0.02)))
+    wd = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, H, I), seed=23, std=0.02)))
+    L = gpu.moe_workspace_layout(T, H, I, E, k)
+    outs = []
+    for fused, keep in ((False, False), (True, False), (True, True)):
+        ws = torch.zeros(L.total, dtype=torch.uint8, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y = gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, four_six=four_six,
+                                   workspace=ws, dev_status=status, fused_h=fused, keep_h=keep)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        R = int(_ws(ws, L, "offsets", np.int32, (E + 1,))[-1])
+        outs.append((to_np(y), _ws(ws, L, "hq_codes", np.uint8, (L.capacity, I // 2))[:R],
+                     _ws(ws, L, "hq_scale", np.float32, (L.capacity,))[:R],
+                     _ws(ws, L, "hq_sf", np.uint8, (L.capacity * (I // 16),))[:R * (I // 16)],
+                     _ws(ws, L, "out", np.uint16, (L.capacity, H))[:R]))
+        if fused and not keep:
+            assert not _ws(ws, L, "h", np.uint16, (L.capacity, I)).any()  # h itself never leaves the scratch
+    for other in outs[1:]:
+        for a, b, what in zip(outs[0], other, ("y", "hq codes", "hq scale", "hq sf", "per-slot outputs")):
+            assert bits_equal(a, b), what
+
+
+def test_moe_fused_h_quantization_bit_identical_full_size(gpu):
+    """The same identity on the Qwen3-30B-A3B-shaped layer (T=16384, H=2048,
+    E=128, top-8, I=768): 576 pair units of six N tiles each."""
+    T, H, I, E, k = 16384, 2048, 768, 128, 8
+    x = synth.normal((T, H), seed=3)
+    ids, wts = synth.topk_routing(T, E, k, seed=3)
+    wgu = gpu.quantize_nvfp4_per_expert(synth.device_normal_bf16((E, 2 * I, H), seed=31, std=0.02))
+    wd = gpu.quantize_nvfp4_per_expert(synth.device_normal_bf16((E, H, I), seed=32, std=0.02))
+    L = gpu.moe_workspace_layout(T, H, I, E, k)
+    res = []
+    for fused in (False, True):
+        ws = torch.zeros(L.total, dtype=torch.uint8, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y = gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, workspace=ws, dev_status=status,
+                                   fused_h=fused)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        R = int(_ws(ws, L, "offsets", np.int32, (E + 1,))[-1])
+        res.append((y.clone(), ws[L.hq_codes:L.hq_codes + R * (I // 2)].clone(),
+                    ws[L.hq_scale:L.hq_scale + 4 * R].clone(), ws[L.hq_sf:L.hq_sf + R * (I // 16)].clone()))
+        del ws
+    for a, b, what in zip(res[0], res[1], ("y", "hq codes", "hq scale", "hq sf")):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.uint8 else a,
+                           b.view(torch.uint8) if b.dtype != torch.uint8 else b), what
