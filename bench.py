@@ -553,7 +553,7 @@ def run_ours(args, w, rank, world, local):
 
     # roofline of the dominant kernel
     dom = max(names, key=lambda n: stage_ms[n])
-    gemm_hash = source_hash("gemm_fp4.cu", "common.cuh")
+    gemm_hash = source_hash("gemm_fp4.cu", "common.cuh", "tc_ptx.cuh")
     if dom in ("gemm1_swiglu", "gemm2"):
         fl = f1 if dom == "gemm1_swiglu" else f2
         ach = fl / (stage_ms[dom] * 1e-3) / 1e12

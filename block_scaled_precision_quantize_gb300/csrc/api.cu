@@ -386,9 +386,11 @@ bsq_status bsq_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, 
     const int64_t cap = moe_capacity(T, E, topk);
     const int64_t nchunks = (T * topk + 511) / 512;  // routing chunk of 512 pairs
     size_t o = 0;
+    // each sub-buffer starts 256-byte aligned and is followed by at least 256
+    // unused bytes, a guard band that tests fill with a canary and check
     auto take = [&](size_t bytes) {
         const size_t at = o;
-        o = align256(o + bytes);
+        o = align256(o + bytes) + 256;
         return at;
     };
     L->capacity = cap;

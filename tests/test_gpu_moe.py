@@ -359,3 +359,39 @@ def test_moe_fused_h_quantization_bit_identical_full_size(gpu):
     for a, b, what in zip(res[0], res[1], ("y", "hq codes", "hq scale", "hq sf")):
         assert torch.equal(a.view(torch.uint8) if a.dtype != torch.uint8 else a,
                            b.view(torch.uint8) if b.dtype != torch.uint8 else b), what
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_moe_workspace_guard_bands(gpu, fused):
+    """Every sub-buffer of the MoE workspace is followed by unused bytes: the
+    forward, run on a workspace filled with a canary byte, must leave all of
+    them, from the end of each sub-buffer's data to the next sub-buffer, as
+    they were (the writes stay inside their buffers, in both GEMM1 paths)."""
+    from conftest import CANARY
+    T, H, I, E, k = 200, 256, 128, 5, 3
+    x = synth.normal((T, H), seed=11)
+    ids, wts = synth.topk_routing(T, E, k, seed=11)
+    wgu = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, 2 * I, H), seed=12, std=0.02)))
+    wd = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, H, I), seed=13, std=0.02)))
+    L = gpu.moe_workspace_layout(T, H, I, E, k)
+    cap = L.capacity
+    ceil4 = lambda n: (n + 3) // 4 * 4  # noqa: E731
+    nchunks = max((T * k + 511) // 512, 1)
+    sizes = {"offsets": (E + 1) * 4, "counts": E * 4, "slot_of": T * k * 4, "row_src": cap * 4,
+             "xq_codes": cap * H // 2, "xq_sf": cap * ceil4(H // 16), "xq_scale": cap * 4, "h": cap * I * 2,
+             "hq_codes": cap * I // 2, "hq_sf": cap * ceil4(I // 16), "hq_scale": cap * 4, "out": cap * H * 2,
+             "scan": (nchunks * E + 1) * 4, "h_scratch": 2 * 256 * 128 * I * 2}
+    fields = sorted(sizes, key=lambda f: getattr(L, f))
+    ws = torch.full((L.total,), CANARY, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, workspace=ws, dev_status=status,
+                           fused_h=fused)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    w = to_np(ws)
+    for f, nxt in zip(fields, fields[1:] + [None]):
+        end = getattr(L, f) + sizes[f]
+        stop = getattr(L, nxt) if nxt else L.total
+        assert stop - end >= 256, f
+        gap = w[end:stop]
+        assert np.all(gap == CANARY), f"write past the end of workspace buffer {f}: {int((gap != CANARY).sum())} bytes"
