@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libbsq.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_fp4.cu", "moe.cu", "ceiling.cu"]
+SOURCES = ["api.cu", "quant.cu", "requant.cu", "gemm_fp4.cu", "moe.cu", "ceiling.cu"]
 HEADERS = ["common.cuh", "kernels.h", "tc_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",

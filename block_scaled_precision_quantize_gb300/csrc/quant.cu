@@ -1,7 +1,7 @@
 // quant.cu -- bandwidth-bound quantizers: per-token / per-expert NVFP4,
-// MXFP8 row+column copies, dequantize-transpose-requantize with Philox
-// stochastic rounding, and small helper kernels (SF layout conversion,
-// format probes, random-bit dumps).
+// MXFP8 row+column copies, the Hadamard-transform and 2-D quantizers, the
+// dequantizer, and small helper kernels (SF layout conversion, format
+// probes, random-bit dumps).  The backward requantization is in requant.cu.
 //
 // Design for GB300: every kernel streams its input once with 16-byte
 // coalesced loads (ld.global.nc, no L1 allocation), reduces maxima with
@@ -413,288 +413,6 @@ __global__ void k_sf_pad_zero(uint8_t* __restrict__ sf, int64_t rows, int64_t co
 }
 
 // ---------------------------------------------------------------------------
-// Requant pass 1: per-column maximum of |D|, D = rn(rn(e2m1 * sf) * t), over
-// all rows.  CTA tile 128 rows x 256 columns, 256 threads: lane l of warp w
-// owns columns 32 (l & 7) .. +31 (one 16-byte code load per row) of rows
-// 4 w + (l >> 3) + 32 i (i = 0..3), all four loads in flight at once; the maxima are folded across the warp by shuffles and across the 8
-// warps in shared memory, and each column's maximum goes to colmax with one
-// unsigned atomicMax on the bits of a non-negative float (order-independent,
-// so the result is deterministic).  colmax must hold zeros beforehand.
-constexpr int RQ1_ROWS = 128, RQ1_COLS = 256;
-
-// The two SF bytes of columns c0 .. c0+31 (c0 a multiple of 32) of row r,
-// packed low = first.
-template <bool SWZ>
-BSQ_DEVICE uint32_t rq_sf_pair(const uint8_t* sf, int64_t r, int64_t c0, int64_t nsf)
-{
-    const int64_t b = c0 >> 4;
-    const int64_t o = SWZ ? sf_swizzled(r, b, (nsf + 3) >> 2) : r * nsf + b;
-    return (uint32_t)__ldg(sf + o) | ((uint32_t)__ldg(sf + o + 1) << 8);  // adjacent in both layouts
-}
-
-template <bool SWZ>
-__global__ void __launch_bounds__(256) k_requant_colmax(const uint8_t* __restrict__ codes,
-                                                        const uint8_t* __restrict__ sf,
-                                                        const float* __restrict__ row_scale, int64_t rows, int64_t K,
-                                                        unsigned int* __restrict__ colmax)
-{
-    pdl_enter();
-    __shared__ float red[8][RQ1_COLS];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t c0 = (int64_t)blockIdx.x * RQ1_COLS + 32 * (lane & 7);
-    const int64_t r0 = (int64_t)blockIdx.y * RQ1_ROWS + 4 * warp + (lane >> 3);
-    const int64_t nsf = K >> 4;
-    float m[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m[i] = 0.0f;
-    if (c0 < K) {  // K % 16 == 0: a 32-column group is whole or half
-        const bool half = c0 + 16 >= K;
-        uint4 w[4];
-        uint32_t sp[4];
-        float t[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t r = r0 + 32 * i;
-            w[i] = make_uint4(0u, 0u, 0u, 0u);
-            sp[i] = 0u;
-            t[i] = 0.0f;
-            if (r < rows) {
-                const uint8_t* p = codes + r * (K >> 1) + (c0 >> 1);
-                if (!half) {
-                    if ((K & 31) == 0) {  // rows 16-byte aligned
-                        w[i] = __ldg(reinterpret_cast<const uint4*>(p));
-                    } else {              // rows 8-byte aligned
-                        const uint2 lo = __ldg(reinterpret_cast<const uint2*>(p));
-                        const uint2 hi = __ldg(reinterpret_cast<const uint2*>(p) + 1);
-                        w[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-                    }
-                    sp[i] = rq_sf_pair<SWZ>(sf, r, c0, nsf);
-                } else {
-                    const uint2 h = __ldg(reinterpret_cast<const uint2*>(p));
-                    w[i] = make_uint4(h.x, h.y, 0u, 0u);
-                    const int64_t o = SWZ ? sf_swizzled(r, c0 >> 4, (nsf + 3) >> 2) : r * nsf + (c0 >> 4);
-                    sp[i] = __ldg(sf + o);
-                }
-                t[i] = __ldg(row_scale + r);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t ww[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float d[8];
-                e2m1x8_dequant(ww[q], (sp[i] >> (8 * (q >> 1))) & 0xFFu, t[i], d);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) m[8 * q + j] = fmaxf(m[8 * q + j], fabsf(d[j]));
-            }
-        }
-    }
-    // fold the four row lanes (l >> 3) of each column group, then the warps
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], 8));
-        m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], 16));
-    }
-    if (lane < 8) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) red[warp][32 * lane + i] = m[i];
-    }
-    __syncthreads();
-    const int64_t c = (int64_t)blockIdx.x * RQ1_COLS + threadIdx.x;
-    float v = red[0][threadIdx.x];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) v = fmaxf(v, red[w][threadIdx.x]);
-    if (c < K && v > 0.0f) atomicMax(colmax + c, __float_as_uint(v));
-}
-
-// Requant pass 2.  CTA tile: 256 source rows (m) x 64 source columns (k),
-// 256 threads.  The tile is dequantized into shared memory transposed,
-// DT[k][m] in binary32: thread m dequantizes source row m (two 16-byte code
-// loads, its four SF bytes and its row scale, all issued up front) and
-// writes column m of DT.  The 4-float chunk c = m >> 2 of a row is stored at
-// chunk c ^ ((c >> 3) & 3), which keeps the 16-byte reads of each
-// quarter-warp below on distinct banks.  Then each half-warp produces one
-// output row k (a source column) per step, warp w taking rows 16 i + 2 w + h:
-// lane l (l16 = l & 15) owns m = 16 l16 .. +15, i.e. one whole NVFP4 block
-// and half of one MXFP8 block (block maximum with its neighbour lane), two
-// Philox calls per format for its 16 random 16-bit draws, and writes 16 + 8
-// contiguous code bytes: each half-warp store covers 256 + 128 contiguous
-// bytes of one output row.  The NVFP4 per-row scales of the tile's rows are
-// computed once per CTA into shared memory.
-constexpr int RQ_TM = 256, RQ_TK = 64;
-
-BSQ_DEVICE int rq_phys(int k, int m)
-{
-    const int c = m >> 2;
-    return k * RQ_TM + 4 * (c ^ ((c >> 3) & 3)) + (m & 3);
-}
-
-// Scale factors of output row k: lane l16 (0..15) of a half-warp holds block
-// col0 + l16 / step of the row (col0 a multiple of 4).  Four consecutive
-// blocks share one 32-bit word when the swizzled layout is used (its column
-// padding absorbs a short last group) or the row length is a multiple of 4;
-// otherwise each block is stored as a byte.  Blocks at or past ncols are not
-// stored.  All 32 lanes must call this (the gathers are warp shuffles; they
-// stay inside each half-warp for the writing lanes).
-BSQ_DEVICE void rq_store_sf(uint8_t* sf, bool swz, int64_t k, int64_t col0, int64_t ncols, uint32_t v, int l16,
-                            int step)
-{
-    const int64_t col = col0 + l16 / step;
-    if (swz || (ncols & 3) == 0) {
-        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, v, step);
-        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, v, 2 * step);
-        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, v, 3 * step);
-        if ((l16 & (4 * step - 1)) == 0 && col < ncols) {
-            const uint32_t word = (v & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) | ((b3 & 0xFFu) << 24);
-            const int64_t off = swz ? sf_swizzled(k, col, (ncols + 3) >> 2) : k * ncols + col;
-            *reinterpret_cast<uint32_t*>(sf + off) = word;
-        }
-    } else if ((l16 & (step - 1)) == 0 && col < ncols) {
-        sf[k * ncols + col] = (uint8_t)v;
-    }
-}
-
-template <bool SWZ, bool SR, bool NV, bool MX>
-__global__ void __launch_bounds__(256) k_requant_main(const uint8_t* __restrict__ codes,
-                                                      const uint8_t* __restrict__ sf,
-                                                      const float* __restrict__ row_scale, int64_t rows, int64_t K,
-                                                      const unsigned int* __restrict__ colmax,
-                                                      uint8_t* __restrict__ nv_codes, uint8_t* __restrict__ nv_sf,
-                                                      float* __restrict__ nv_scale, uint8_t* __restrict__ mx_codes,
-                                                      uint8_t* __restrict__ mx_sf, const PhiloxKeys keys)
-{
-    pdl_enter();
-    extern __shared__ __align__(16) float DT[];  // [RQ_TK][RQ_TM]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t m0 = (int64_t)blockIdx.y * RQ_TM, k0 = (int64_t)blockIdx.x * RQ_TK;
-    const int64_t nsf_in = K >> 4;
-    {
-        // dequantize source row m = tid, columns k0 .. k0+63 (K % 16 == 0)
-        const int m = tid;
-        const int64_t gm = m0 + m;
-        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        uint32_t sfw = 0u;
-        float t = 0.0f;
-        const int64_t nw_all = (K - k0) >> 3;
-        const int nw = nw_all < 8 ? (int)nw_all : 8;  // code words of 8 columns in range
-        if (gm < rows) {
-            const uint8_t* p = codes + gm * (K >> 1) + (k0 >> 1);
-            if (nw == 8 && (K & 31) == 0) {  // rows 16-byte aligned
-                const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-                const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            } else if (nw == 8) {            // rows 8-byte aligned
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint2 h = __ldg(reinterpret_cast<const uint2*>(p) + i);
-                    w[2 * i] = h.x;
-                    w[2 * i + 1] = h.y;
-                }
-            } else {
-                for (int i = 0; i < nw; ++i) w[i] = __ldg(reinterpret_cast<const uint32_t*>(p) + i);
-            }
-            const int64_t b0 = k0 >> 4;  // first SF column (a multiple of 4)
-            const int64_t o = SWZ ? sf_swizzled(gm, b0, (nsf_in + 3) >> 2) : gm * nsf_in + b0;
-            if (nw == 8 && (SWZ || (nsf_in & 3) == 0)) {
-                sfw = __ldg(reinterpret_cast<const uint32_t*>(sf + o));
-            } else {
-                for (int i = 0; i < (nw + 1) / 2; ++i) sfw |= (uint32_t)__ldg(sf + o + i) << (8 * i);
-            }
-            t = __ldg(row_scale + gm);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float d[8];
-            e2m1x8_dequant(w[q], (sfw >> (8 * (q >> 1))) & 0xFFu, t, d);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) DT[rq_phys(8 * q + j, m)] = d[j];
-        }
-    }
-    __shared__ float tq[RQ_TK];  // NVFP4 per-row scales of the tile's output rows
-    if (NV && tid < RQ_TK) {
-        const int64_t gk = k0 + tid;
-        float t = 0.0f;
-        if (gk < K) {
-            t = __fdiv_rn(__uint_as_float(__ldg(colmax + gk)), kNvfp4ScaleDivisor);
-            if (blockIdx.y == 0) nv_scale[gk] = t;
-        }
-        tq[tid] = t;
-    }
-    __syncthreads();
-    const int l16 = lane & 15, half = lane >> 4;
-    const int64_t gm = m0 + 16 * l16;   // first source row of this lane
-    const bool valid = gm < rows;        // rows % 32 == 0: whole MXFP8 blocks drop out
-    for (int it = 0; it < RQ_TK / 16; ++it) {
-        const int kk = 16 * it + 2 * warp + half;
-        const int64_t gk = k0 + kk;
-        if (k0 + 16 * it >= K) break;   // K % 16 == 0: the 16 rows of a step are all in or all out
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 a = *reinterpret_cast<const float4*>(DT + rq_phys(kk, 16 * l16 + 4 * j));
-            v[4 * j] = a.x; v[4 * j + 1] = a.y; v[4 * j + 2] = a.z; v[4 * j + 3] = a.w;
-        }
-        float am = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
-        const uint64_t g8 = ((uint64_t)gk * (uint64_t)rows + (uint64_t)gm) >> 3;  // Philox counter of v[0..7]
-        if (MX) {
-            const float ab = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));  // MXFP8 block (32 rows)
-            uint32_t w[4] = {0u, 0u, 0u, 0u}, sc = 0u;
-            if (ab > 0.0f) {
-                const int X = mx_exponent(__float_as_uint(ab));
-                const float mul = mx_multiplier(X);
-                sc = (uint32_t)(X + 127);
-                if (SR) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 rb = sr_block_bits_keys(keys, 1u, g8 + h);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            w[2 * h + (j >> 2)] |= e4m3_sr(__fmul_rn(v[8 * h + j], mul), sr_pick16(rb, j)) << (8 * (j & 3));
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        w[q] = e4m3x4(__fmul_rn(v[4 * q], mul), __fmul_rn(v[4 * q + 1], mul), __fmul_rn(v[4 * q + 2], mul),
-                                      __fmul_rn(v[4 * q + 3], mul));
-                }
-            }
-            if (valid) *reinterpret_cast<uint4*>(mx_codes + gk * rows + gm) = make_uint4(w[0], w[1], w[2], w[3]);
-            rq_store_sf(mx_sf, SWZ, gk, m0 >> 5, rows >> 5, sc, l16, 2);
-        }
-        if (NV) {
-            const float t = tq[kk];
-            uint32_t w[2] = {0u, 0u}, sfb = 0u;
-            if (t != 0.0f) {
-                const BlockScale bs = nvfp4_block_scale(am, __fmul_rn(6.0f, t), t);
-                sfb = bs.sf;
-                if (SR) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 rb = sr_block_bits_keys(keys, 0u, g8 + h);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) w[h] |= e2m1_sr(__fmul_rn(v[8 * h + j], bs.enc), sr_pick16(rb, j)) << (4 * j);
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        w[h] = e2m1x8(__fmul_rn(v[8 * h], bs.enc), __fmul_rn(v[8 * h + 1], bs.enc),
-                                      __fmul_rn(v[8 * h + 2], bs.enc), __fmul_rn(v[8 * h + 3], bs.enc),
-                                      __fmul_rn(v[8 * h + 4], bs.enc), __fmul_rn(v[8 * h + 5], bs.enc),
-                                      __fmul_rn(v[8 * h + 6], bs.enc), __fmul_rn(v[8 * h + 7], bs.enc));
-                }
-            }
-            if (valid) *reinterpret_cast<uint2*>(nv_codes + gk * (rows >> 1) + (gm >> 1)) = make_uint2(w[0], w[1]);
-            rq_store_sf(nv_sf, SWZ, gk, m0 >> 4, rows >> 4, sfb, l16, 1);
-        }
-    }
-}
-constexpr size_t RQ_SMEM = (size_t)RQ_TM * RQ_TK * sizeof(float);  // 64 KB
-
-// ---------------------------------------------------------------------------
 // Helpers.
 __global__ void k_sf_swizzle(const uint8_t* __restrict__ in, int64_t rows, int64_t cols, uint8_t* __restrict__ out,
                              int dir)
@@ -850,53 +568,6 @@ void launch_sf_pad_zero(uint8_t* sf, int64_t rows, int64_t cols, int sms, cudaSt
     k_sf_pad_zero<<<sms * 4, 256, 0, st>>>(sf, rows, cols);
 }
 
-// Both requant passes; colmax (K words) is cleared here when NVFP4 output is wanted.
-template <bool S, bool R, bool N, bool M>
-static cudaError_t requant_main(dim3 grid, const uint8_t* codes, const uint8_t* sf, const float* row_scale,
-                                int64_t rows, int64_t K, const unsigned int* colmax, uint8_t* nvc, uint8_t* nvs,
-                                float* nvt, uint8_t* mxc, uint8_t* mxs, uint64_t seed, cudaStream_t st)
-{
-    static std::atomic<uint64_t> attr_done{0};
-    cudaError_t err = once_per_device(attr_done, [] {
-        return cudaFuncSetAttribute(k_requant_main<S, R, N, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)RQ_SMEM);
-    });
-    if (err != cudaSuccess) return err;
-    launch_ks(k_requant_main<S, R, N, M>, grid, dim3(256), RQ_SMEM, true, st, codes, sf, row_scale, rows, K, colmax,
-              nvc, nvs, nvt, mxc, mxs, philox_keys(seed));
-    return cudaGetLastError();
-}
-
-static cudaError_t requant_passes(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
-                                  int64_t K, unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc,
-                                  uint8_t* mxs, uint64_t seed, bool sr, bool swz, cudaStream_t st)
-{
-    const bool nv = nvc != nullptr, mx = mxc != nullptr;
-    if (nv) {
-        cudaError_t err = cudaMemsetAsync(colmax, 0, (size_t)K * sizeof(unsigned int), st);
-        if (err != cudaSuccess) return err;
-        dim3 g1((unsigned)((K + RQ1_COLS - 1) / RQ1_COLS), (unsigned)((rows + RQ1_ROWS - 1) / RQ1_ROWS));
-        if (swz) launch_k(k_requant_colmax<true>, g1, dim3(256), true, st, codes, sf, row_scale, rows, K, colmax);
-        else launch_k(k_requant_colmax<false>, g1, dim3(256), true, st, codes, sf, row_scale, rows, K, colmax);
-    }
-    dim3 g2((unsigned)((K + RQ_TK - 1) / RQ_TK), (unsigned)((rows + RQ_TM - 1) / RQ_TM));
-#define BSQ_RQ(S, R, N, M) \
-    requant_main<S, R, N, M>(g2, codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, st)
-#define BSQ_RQ2(S, R)                                                                                 \
-    (nv && mx ? BSQ_RQ(S, R, true, true) : nv ? BSQ_RQ(S, R, true, false) : BSQ_RQ(S, R, false, true))
-    if (swz) return sr ? BSQ_RQ2(true, true) : BSQ_RQ2(true, false);
-    return sr ? BSQ_RQ2(false, true) : BSQ_RQ2(false, false);
-#undef BSQ_RQ2
-#undef BSQ_RQ
-}
-
-cudaError_t launch_requant(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows, int64_t K,
-                           unsigned int* colmax, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
-                           uint64_t seed, bool sr, bool swz, cudaStream_t st)
-{
-    return requant_passes(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, sr, swz, st);
-}
-
 void launch_sf_swizzle(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, int dir, int sms,
                        cudaStream_t st)
 {
@@ -913,59 +584,6 @@ void launch_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t
                           cudaStream_t st)
 {
     k_philox_bits16<<<sms * 8, 256, 0, st>>>(seed, stream, idx0, n, out);
-}
-
-// ---------------------------------------------------------------------------
-// Allocation-free requantization (requant_transpose_sr_noalloc).
-//
-// Some callers cannot give the library device memory for scratch: a host
-// framework that only owns its input and output buffers, or code that must
-// not allocate device memory once it is running.  For them the column maxima
-// of |D| live in this file-scope device array instead of a caller workspace.
-// Every GPU that loads the library holds it (256 KB) until the process exits,
-// every call shares it, and it keeps the last call's contents, so each call
-// clears the part it uses first; calls that overlap on the GPU (different
-// streams, or different host threads on one device) race on it.
-namespace {
-
-constexpr int64_t kNoallocMaxK = 65536;
-__device__ __align__(256) unsigned int g_requant_colmax[kNoallocMaxK];
-
-// Device address of g_requant_colmax, looked up once per device with that
-// device current (the host-side name is only a stand-in for it).
-constexpr int kNoallocDevices = 64;
-std::mutex g_noalloc_mutex;
-unsigned int* g_noalloc_ptr[kNoallocDevices];
-
-cudaError_t noalloc_scratch(unsigned int** out)
-{
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kNoallocDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_requant_colmax);
-        if (err != cudaSuccess) return err;
-        g_noalloc_ptr[dev] = static_cast<unsigned int*>(p);
-    }
-    *out = g_noalloc_ptr[dev];
-    return cudaSuccess;
-}
-
-}  // namespace
-
-int64_t noalloc_requant_max_k() { return kNoallocMaxK; }
-
-cudaError_t launch_requant_noalloc(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t rows,
-                                   int64_t K, uint8_t* nvc, uint8_t* nvs, float* nvt, uint8_t* mxc, uint8_t* mxs,
-                                   uint64_t seed, bool sr, bool swz, cudaStream_t st)
-{
-    unsigned int* colmax = nullptr;
-    cudaError_t err = noalloc_scratch(&colmax);
-    if (err != cudaSuccess) return err;
-    return requant_passes(codes, sf, row_scale, rows, K, colmax, nvc, nvs, nvt, mxc, mxs, seed, sr, swz, st);
 }
 
 // ---------------------------------------------------------------- RHT + NVFP4
