@@ -631,6 +631,11 @@ def run_ours(args, w, rank, world, local):
 
     components = {} if args.no_components else {**quantizer_components(bsq, synth, dev, P),
                                                  **backward_gemm_components(bsq, dev, P)}
+    # the other layer shape the pages run (DeepSeek-V3-shaped, 4/6 on the
+    # activations) as a second record, when this run is the Qwen3 one
+    second = None
+    if not args.no_components and args.workload == "qwen3" and world == 1:
+        second = layer_record(bsq, synth, WORKLOADS["deepseek"], dev, P)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -641,12 +646,84 @@ def run_ours(args, w, rank, world, local):
                        "l2": "working set ~1 GB > 129 MB L2; no flush between steps; components rotate input sets > 2x L2",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "mma_ceiling": ceiling, "stages": stages, "components": components, "e2e": e2e,
-            "step_with_h_quantized_in_gemm1_ms": fused_h_ms,
+            "step_with_h_quantized_in_gemm1_ms": fused_h_ms, "second_record": second,
             "gpu_launches": KERNELS_PER_STEP * K, "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x_bits, ids)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def layer_record(bsq, synth, w, dev, P, steps=10, warmup=3):
+    """Step time and per-stage breakdown of one MoE layer workload `w` (the
+    second record of the bench line): inputs and weights generated on the
+    device, `steps` forwards timed back to back with CUDA events, then the
+    same number with events at the stage boundaries."""
+    import torch
+    T, H, I, E, k = w["T"], w["H"], w["I"], w["E"], w["k"]
+    four_six = w.get("four_six", False)
+    x = torch.from_numpy(synth.normal((T, H), seed=w["seed"]).view(np.int16)).view(torch.bfloat16).to(dev)
+    ids, wts = synth.topk_routing(T, E, k, seed=w["seed"], zipf_s=w.get("zipf"))
+    ids_d, wts_d = torch.from_numpy(ids).to(dev), torch.from_numpy(wts).to(dev)
+    wb = synth.device_normal_bf16((E, 2 * I, H), seed=w["w_seed_gu"], std=0.02, device=dev)
+    wgu = bsq.quantize_nvfp4_per_expert(wb)
+    del wb
+    wb = synth.device_normal_bf16((E, H, I), seed=w["w_seed_d"], std=0.02, device=dev)
+    wd = bsq.quantize_nvfp4_per_expert(wb)
+    del wb
+    ws = torch.empty(bsq.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def fwd():
+        bsq.moe_expert_forward(x, ids_d, wts_d, wgu, wd, I, four_six=four_six, workspace=ws, y=y, dev_status=status)
+
+    for _ in range(warmup):
+        fwd()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fwd()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for row in ev:  # torch creates an event's CUDA handle at its first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        bsq.set_stage_events(ev[i])
+        fwd()
+    bsq.set_stage_events(None)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    names = ["route", "quantize_scatter", "gemm1_swiglu", "quantize_h", "gemm2", "combine"]
+    stage_ms = {n: statistics.mean(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(steps))
+                for s, n in enumerate(names)}
+    f1, f2 = gemm_flops(w)
+    R = T * k
+    L = bsq.moe_workspace_layout(T, H, I, E, k)
+    R_pad = int(ws[L.offsets + 4 * E:L.offsets + 4 * (E + 1)].view(torch.int32).item())
+    stage_bytes = {"quantize_scatter": T * H * 2 + R * (H // 2 + H // 16 + 4),
+                   "quantize_h": R_pad * I * 2 + R_pad * (I // 2 + I // 16 + 4),
+                   "combine": R * H * 2 + T * H * 2 + R * 8}
+    stages = {}
+    for n in names:
+        d = {"ms": stage_ms[n]}
+        if n in ("gemm1_swiglu", "gemm2"):
+            d["tflops"] = (f1 if n == "gemm1_swiglu" else f2) / (stage_ms[n] * 1e-3) / 1e12
+            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops"]
+        elif n in stage_bytes:
+            d["gbs"] = stage_bytes[n] / (stage_ms[n] * 1e-3) / 1e9
+            d["frac_of_hbm"] = d["gbs"] / P["hbm_gbs"]
+        stages[n] = d
+    del x, ids_d, wts_d, wgu, wd, ws, y
+    torch.cuda.empty_cache()
+    return {"workload": w["name"], "metric": METRIC, "value": (f1 + f2) / (ms_step * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "ms_per_step": ms_step, "steps": steps, "warmup": warmup, "four_six": four_six,
+            "routed_rows": R, "padded_rows": R_pad, "gemm_tflop_per_step": (f1 + f2) / 1e12, "stages": stages}
 
 
 def time_rotating(launch, nsets, iters):

@@ -94,6 +94,8 @@ def set_stage_events(events):
         _stage_array = None
         _check(load().bsq_set_stage_events(None, 0), "bsq_set_stage_events")
         return
+    if any(not e.cuda_event for e in events):
+        raise ValueError("set_stage_events: record each event once first (torch creates the CUDA event lazily)")
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _stage_array = arr  # keep alive while set
     _check(load().bsq_set_stage_events(arr, len(events)), "bsq_set_stage_events")

@@ -134,21 +134,33 @@ BSQ_DEVICE void e2m1x8_f16x2(uint32_t w, uint32_t (&h)[4])
         : "r"(w));
 }
 
-// The NVFP4 block scale E4M3(rn(amax / rn(6 t))) from q = rn(amax * inv6),
-// inv6 = rn(1 / rn(6 t)): q is within 1.5 units in the last place of the
-// exact quotient, so when q (1 - 2^-20) and q (1 + 2^-20) encode to the same
-// E4M3 byte (E4M3 rounding is monotone), so does the correctly rounded
-// quotient; otherwise (q near a rounding boundary, or inv6 = 0 marking a row
-// whose reciprocal would overflow) the quotient is computed exactly.
-BSQ_DEVICE uint32_t nv_block_sf(float amax, float six_t, float inv6)
+// rn(1 / m) for e4m3_of_quotient, or 0 where that quotient is to be taken
+// exactly: m zero or non-finite, or a reciprocal outside the normal range
+// (there its relative error is not bounded by one unit in the last place).
+BSQ_DEVICE float quotient_inv(float m)
 {
-    const float q = __fmul_rn(amax, inv6);
+    const float r = __frcp_rn(m);
+    return (r >= 1.17549435e-38f && r <= kFltMax) ? r : 0.0f;
+}
+
+// The NVFP4 block scale E4M3(rn(a / m)) (RNE, satfinite; a = the block's
+// amax, m = rn(6 t)) given inv = quotient_inv(m).  q = rn(a * inv) lies
+// within 1.5 units in the last place of a / m, so when q (1 - 2^-20) and
+// q (1 + 2^-20) encode to the same byte -- E4M3 rounding is monotone -- so
+// does the correctly rounded quotient; otherwise (q near an E4M3 rounding
+// boundary, or inv = 0) the quotient is computed exactly.  Here the divisor
+// changes with every output row, so a division per block would not be
+// hoisted; this costs one multiply, two scalings and one conversion in all
+// but a few blocks in 10^5.
+BSQ_DEVICE uint32_t e4m3_of_quotient(float a, float m, float inv)
+{
+    const float q = __fmul_rn(a, inv);
     uint32_t two;
     asm("{\n\t.reg .b16 b;\n\tcvt.rn.satfinite.e4m3x2.f32 b, %1, %2;\n\tcvt.u32.u16 %0, b;\n\t}"
         : "=r"(two)
         : "f"(__fmul_rn(q, 1.00000095367431640625f)), "f"(__fmul_rn(q, 0.99999904632568359375f)));
-    if (inv6 != 0.0f && (two & 0xFFu) == (two >> 8)) return two & 0xFFu;
-    return e4m3_rn(__fdiv_rn(amax, six_t));
+    if (inv != 0.0f && (two & 0xFFu) == (two >> 8)) return two & 0xFFu;
+    return e4m3_rn(__fdiv_rn(a, m));
 }
 
 // Two E4M3 bytes (low = first) -> f16x2.
@@ -322,7 +334,7 @@ __global__ void __launch_bounds__(256) k_rq_tile(const uint8_t* __restrict__ cod
     pdl_enter();
     __shared__ __align__(16) uint32_t DT[RT_K * (RT_M / 2)];  // 32 KB
     __shared__ __align__(16) float tsrc[RT_M];
-    __shared__ float4 tq[RT_K];  // (t, rn(6 t), rn(1 / rn(6 t)) or 0) of the NVFP4 output rows
+    __shared__ float4 tq[RT_K];  // (t, rn(6 t), quotient_inv(rn(6 t))) of the NVFP4 output rows
     __shared__ __align__(16) uint8_t sfo_nv[RT_K][RT_M / 16];
     __shared__ __align__(16) uint8_t sfo_mx[RT_K][RT_M / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -402,8 +414,7 @@ __global__ void __launch_bounds__(256) k_rq_tile(const uint8_t* __restrict__ cod
                 if (blockIdx.y == 0) nv_scale[gk] = t;
             }
             const float six = __fmul_rn(6.0f, t);
-            const float inv = six != 0.0f ? __frcp_rn(six) : 0.0f;
-            tq[tid] = make_float4(t, six, isinf(inv) ? 0.0f : inv, 0.0f);
+            tq[tid] = make_float4(t, six, quotient_inv(six), 0.0f);
         }
     }
     __syncthreads();
@@ -470,7 +481,7 @@ __global__ void __launch_bounds__(256) k_rq_tile(const uint8_t* __restrict__ cod
             uint32_t w[2] = {0u, 0u}, sfb = 0u;
             if (tt.x != 0.0f) {
                 BlockScale bs;
-                bs.sf = nv_block_sf(am, tt.y, tt.z);
+                bs.sf = e4m3_of_quotient(am, tt.y, tt.z);
                 bs.d = __fmul_rn(f16lo_to_f32(e4m3x2_f16x2(bs.sf)), tt.x);
                 const float enc = bs.d == 0.0f ? 0.0f : __frcp_rn(bs.d);
                 bs.enc = isinf(enc) ? kFltMax : enc;
