@@ -606,9 +606,22 @@ void launch_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, int64_t
 // three, so occupancy is not what bounds it.
 namespace {
 
-BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int b0, int lane, uint32_t signs,
+// The sign flips of this lane's 16 elements (its block's half of the
+// group) as XOR masks on the 8 packed bf16 words: element 2 j is the low half
+// of word j (sign bit 15), element 2 j + 1 the high half (bit 31).
+BSQ_DEVICE void rht_sign_masks(uint32_t signs, int lane, uint32_t (&m)[8])
+{
+    const uint32_t sg = (lane & 1) ? (signs >> 16) : signs;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = (((sg >> (2 * j)) & 1u) << 15) | (((sg >> (2 * j + 1)) & 1u) << 31);
+}
+
+BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int b0, int lane, const uint32_t (&sm)[8],
                            float (&v)[2][16])
 {
+    // the cross-lane stage: the even lane of a pair keeps v + o, the odd lane
+    // o - v; fma(+-1, v, o) rounds the same sum or difference once
+    const float pm = (lane & 1) ? -1.0f : 1.0f;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int b = b0 + lane + 32 * i;
@@ -618,12 +631,11 @@ BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int b0, in
             c = ldg_stream(xr + 16 * b + 8);
         }
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-        const uint32_t sg = (lane & 1) ? (signs >> 16) : signs;  // this block's half of the group
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-            v[i][2 * j] = ((sg >> (2 * j)) & 1u) ? -lo : lo;
-            v[i][2 * j + 1] = ((sg >> (2 * j + 1)) & 1u) ? -hi : hi;
+            const uint32_t ws = w[j] ^ sm[j];  // s . x: bf16 negation is a sign-bit flip
+            v[i][2 * j] = bf16_lo(ws);
+            v[i][2 * j + 1] = bf16_hi(ws);
         }
 #pragma unroll
         for (int h = 1; h < 16; h <<= 1)
@@ -637,7 +649,7 @@ BSQ_DEVICE void rht_blocks(const uint16_t* __restrict__ xr, int nblk, int b0, in
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i][j], 1);
-            v[i][j] = (lane & 1) ? __fsub_rn(o, v[i][j]) : __fadd_rn(v[i][j], o);
+            v[i][j] = __fmaf_rn(pm, v[i][j], o);
         }
     }
 }
@@ -655,6 +667,8 @@ __global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict
     const int64_t nct = (ncol_pad + 3) >> 2;
     const int64_t rows_iter = SWZ ? ((rows + 127) & ~(int64_t)127) : rows;
     const uint32_t signs = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32)).x;
+    uint32_t sm[8];
+    rht_sign_masks(signs, lane, sm);
     // CTA-uniform loop over groups of 4 rows (the shared-memory fold synchronizes the CTA)
     for (int64_t r0 = (int64_t)blockIdx.x * 4; r0 < rows_iter; r0 += (int64_t)gridDim.x * 4) {
         const int64_t r = r0 + (warp >> 1);
@@ -663,7 +677,7 @@ __global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict
         float v[2][16];
         float amax = 0.0f;
         for (int c0 = 0; c0 < nblk; c0 += 128) {  // one chunk for rows of up to 128 blocks
-            if (real) rht_blocks(xr, nblk, c0 + 64 * half, lane, signs, v);
+            if (real) rht_blocks(xr, nblk, c0 + 64 * half, lane, sm, v);
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -684,7 +698,7 @@ __global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict
         const float six_t = __fmul_rn(6.0f, t);
         uint2* crow = reinterpret_cast<uint2*>(codes + r * (K >> 1));
         for (int c0 = 0; c0 < nblk; c0 += 128) {
-            if (nblk > 128) rht_blocks(xr, nblk, c0 + 64 * half, lane, signs, v);  // second pass: transform again
+            if (nblk > 128) rht_blocks(xr, nblk, c0 + 64 * half, lane, sm, v);  // second pass: transform again
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int b = c0 + 64 * half + lane + 32 * i;
@@ -728,18 +742,21 @@ void launch_nvfp4_rht(const uint16_t* x, int64_t rows, int64_t K, int64_t ldx, u
 // before and after the transpose, so the transposed backward operand is the
 // same codes and scales rearranged, with no requantization; the price is 256
 // values under one scale).
-// Pass 1, the tensor maximum: grid-stride 16-byte loads, folded per warp and
-// per CTA, one atomic per CTA.
+// Pass 1, the tensor maximum: grid-stride 16-byte loads, 8 in flight per
+// thread, folded per warp and per CTA, one atomic per CTA.
 // Pass 2: a CTA takes 128 rows x 128 columns; warp w the 16-row strip w of
 // it.  Lanes 4p .. 4p + 3 take 4 columns each of tile p over its 16 rows
 // (8-byte loads: every load instruction reads 256 contiguous bytes of a row,
-// and 32 registers hold the data); the tile maximum is folded over the four
-// lanes.  The row-major codes leave as 2 bytes per lane and row (64
-// contiguous bytes per instruction).  The transposed codes (8 bytes = 16 rows
-// per column and strip) meet in shared memory, in 72-byte rows with the strip
-// slot rotated by column so that a warp's 256 bytes take the minimum two
-// wavefronts; two threads then write each column's 64 bytes (the CTA's 128
-// rows) of the transposed operand, 32 bytes each.
+// and 32 registers hold the data); the tile maximum (packed bf16 |max|) is
+// folded over the four lanes.  The row-major codes leave as 2 bytes per lane
+// and row (64 contiguous bytes per instruction).  For the transposed codes
+// (8 bytes = 16 rows per column and strip) the code words of rows 4g, 4g + 2
+// and 4g + 1, 4g + 3 are packed in pairs and interleaved by nibble, which
+// puts each column's row pairs in bytes; one byte permute per column and 8
+// rows gathers them.  They meet in shared memory, in 72-byte rows with the
+// strip slot rotated by column so that a warp's 256 bytes take the minimum
+// two wavefronts; two threads then write each column's 64 bytes (the CTA's
+// 128 rows) of the transposed operand, 32 bytes each.
 namespace {
 
 __global__ void __launch_bounds__(256) k_tensor_amax(const uint16_t* __restrict__ x, int64_t n8,
@@ -749,10 +766,11 @@ __global__ void __launch_bounds__(256) k_tensor_amax(const uint16_t* __restrict_
     uint32_t m = 0;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 7 * stride < n8; i += 8 * stride) {
+    for (; i < n8; i += 8 * stride) {  // 8 loads in flight, the tail predicated
         uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = ldg_stream(x + 8 * (i + u * stride));
+        for (int u = 0; u < 8; ++u)
+            v[u] = i + u * stride < n8 ? ldg_stream(x + 8 * (i + u * stride)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             uint32_t a = absmax_bf16x2(0u, v[u].x);
@@ -762,14 +780,6 @@ __global__ void __launch_bounds__(256) k_tensor_amax(const uint16_t* __restrict_
             m = max(m, fold_halves(a));
         }
     }
-    for (; i < n8; i += stride) {
-        const uint4 v = ldg_stream(x + 8 * i);
-        uint32_t a = absmax_bf16x2(0u, v.x);
-        a = absmax_bf16x2(a, v.y);
-        a = absmax_bf16x2(a, v.z);
-        a = absmax_bf16x2(a, v.w);
-        m = max(m, fold_halves(a));
-    }
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -777,6 +787,20 @@ __global__ void __launch_bounds__(256) k_tensor_amax(const uint16_t* __restrict_
         for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_m[w]);
         if (m) atomicMax(amax_bits, m << 16);
     }
+}
+
+// Four binary32 values -> four E2M1 codes in the low 16 bits (element i in
+// nibble i), RNE satfinite.
+BSQ_DEVICE uint32_t e2m1x4_16(float v0, float v1, float v2, float v3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1;\n\t.reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "mov.b16 h, {b0, b1};\n\tcvt.u32.u16 %0, h;\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
 }
 
 template <bool T_OUT>
@@ -798,12 +822,14 @@ __global__ void __launch_bounds__(256) k_nvfp4_2d(const uint16_t* __restrict__ x
         const int64_t r0 = R0 + 16 * warp, c0 = C0 + 4 * lane;  // this lane's first row and column
         const bool valid = r0 < rows && c0 < K;                  // K % 16 == 0: the lanes of a tile agree
         uint2 v[16];
-        uint32_t m = 0;
+        uint32_t m2 = 0;  // packed bf16 max of |x| (sign bits meaningless until masked)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             v[i] = valid ? __ldcs(reinterpret_cast<const uint2*>(x + (r0 + i) * K + c0)) : make_uint2(0u, 0u);
-            m = max(m, fold_halves(absmax_bf16x2(absmax_bf16x2(0u, v[i].x), v[i].y)));
+            asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v[i].x));
+            asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v[i].y));
         }
+        uint32_t m = fold_halves(m2 & 0x7FFF7FFFu);
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
         uint32_t sfb = 0u;
@@ -816,24 +842,29 @@ __global__ void __launch_bounds__(256) k_nvfp4_2d(const uint16_t* __restrict__ x
         uint32_t w[16];  // 4 codes (16 bits) of row i
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            w[i] = (t != 0.0f) ? (e2m1x8(__fmul_rn(bf16_lo(v[i].x), enc), __fmul_rn(bf16_hi(v[i].x), enc),
-                                         __fmul_rn(bf16_lo(v[i].y), enc), __fmul_rn(bf16_hi(v[i].y), enc), 0.0f, 0.0f,
-                                         0.0f, 0.0f) & 0xFFFFu)
+            w[i] = (t != 0.0f) ? e2m1x4_16(__fmul_rn(bf16_lo(v[i].x), enc), __fmul_rn(bf16_hi(v[i].x), enc),
+                                           __fmul_rn(bf16_lo(v[i].y), enc), __fmul_rn(bf16_hi(v[i].y), enc))
                                : 0u;
             if (valid) *reinterpret_cast<uint16_t*>(codes + (r0 + i) * (K >> 1) + (c0 >> 1)) = (uint16_t)w[i];
         }
         if (valid && (lane & 3) == 0) sf[(r0 >> 4) * (K >> 4) + (c0 >> 4)] = (uint8_t)sfb;
         if constexpr (T_OUT) {
+            // rows 4g, 4g + 1 (bytes 0, 1) and 4g + 2, 4g + 3 (bytes 2, 3) of
+            // columns 0, 2 (ev) and 1, 3 (od): row 4g + 2k in the low nibble
+            uint32_t ev[4], od[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint32_t wa = __byte_perm(w[4 * g], w[4 * g + 2], 0x5410u);
+                const uint32_t wb = __byte_perm(w[4 * g + 1], w[4 * g + 3], 0x5410u);
+                ev[g] = (wa & 0x0F0F0F0Fu) | ((wb << 4) & 0xF0F0F0F0u);
+                od[g] = ((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u);
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    lo |= ((w[i] >> (4 * j)) & 0xFu) << (4 * i);
-                    hi |= ((w[i + 8] >> (4 * j)) & 0xFu) << (4 * i);
-                }
+                const uint32_t* q = (j & 1) ? od : ev;
+                const uint32_t sel = (j & 2) ? 0x7531u : 0x6420u;  // columns 2, 3: the odd bytes
                 const int col = 4 * lane + j;
-                s_t[col][(warp + (col >> 4)) & 7] = make_uint2(lo, hi);
+                s_t[col][(warp + (col >> 4)) & 7] = make_uint2(__byte_perm(q[0], q[1], sel), __byte_perm(q[2], q[3], sel));
             }
             if ((lane & 3) == 0) s_sf[lane >> 2][warp] = (uint8_t)sfb;
             __syncthreads();
