@@ -253,9 +253,15 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
         if (!real) continue;
         const float tt = __fdiv_rn(bf16mag_to_f32(rmax), kNvfp4ScaleDivisor);
         const float six_t = __fmul_rn(6.0f, tt), four_t = __fmul_rn(4.0f, tt);
-        // lane j < topk holds the slot of pair (t, j) (-1: not routed)
+        // lane j < topk holds the slot of pair (t, j) (-1: not routed), and
+        // that slot row's byte offsets: codes, and the row part of the
+        // swizzled SF address (the block's column part is fixed per lane)
         const int32_t my_slot = lane < topk ? __ldg(slot_of + t * topk + lane) : -1;
         if (my_slot >= 0 && part == 0) scale[my_slot] = tt;
+        const int64_t my_crow = (int64_t)(my_slot < 0 ? 0 : my_slot) * (H >> 1);
+        const int64_t my_srow = my_slot < 0 ? 0 : sf_swizzled(my_slot, 0, ncol_tiles);
+        uint2 cw[BPL];
+        uint32_t sw[BPL];
 #pragma unroll
         for (int i = 0; i < BPL; ++i) {
             const int b = li + 32 * WPR * i;
@@ -287,12 +293,25 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
             const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, s, 1);
             const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, s, 2);
             const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, s, 3);
-            const uint32_t sw = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
-            for (int j = 0; j < topk; ++j) {
-                const int32_t r = __shfl_sync(0xFFFFFFFFu, my_slot, j);
-                if (r < 0 || b >= nblk) continue;
-                reinterpret_cast<uint2*>(codes + (int64_t)r * (H >> 1))[b] = c;
-                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_swizzled(r, b, ncol_tiles)) = sw;
+            cw[i] = c;
+            sw[i] = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+        // each routed slot: its code row, and the column part (b / 4) * 512 +
+        // b % 4 of each block's swizzled SF address (b % 4 == 0 at the storing
+        // lanes)
+        for (int j = 0; j < topk; ++j) {
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_slot, j);
+            if (r < 0) continue;  // warp-uniform
+            const int64_t crow = __shfl_sync(0xFFFFFFFFu, my_crow, j);
+            const int64_t srow = __shfl_sync(0xFFFFFFFFu, my_srow, j);
+            uint2* cdst = reinterpret_cast<uint2*>(codes + crow);
+            uint8_t* sdst = sf + srow;
+#pragma unroll
+            for (int i = 0; i < BPL; ++i) {
+                const int b = li + 32 * WPR * i;
+                if (b >= nblk) continue;
+                cdst[b] = cw[i];
+                if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sdst + (b >> 2) * 512) = sw[i];
             }
         }
     }
