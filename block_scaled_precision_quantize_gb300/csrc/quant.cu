@@ -689,11 +689,8 @@ __global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict
         amax = fmaxf(s_max[warp & ~1], s_max[warp | 1]);
         __syncthreads();
         if (r >= rows_iter) continue;
-        // this row's part of its SF addresses; block b adds (b / 4) * 512 + b % 4
-        // in the swizzled layout, b in the row-major one
-        uint8_t* const srow = sf + (SWZ ? sf_swizzled(r, 0, nct) : r * nblk);
         if (!real) {  // swizzle padding rows: zero scale factors
-            for (int b = 32 * half + lane; b < ncol_pad; b += 64) srow[(b >> 2) * 512 + (b & 3)] = 0u;
+            for (int b = 32 * half + lane; b < ncol_pad; b += 64) sf[sf_swizzled(r, b, nct)] = 0u;
             continue;
         }
         const float t = __fdiv_rn(amax, kNvfp4ScaleDivisor);
@@ -706,7 +703,7 @@ __global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict
             for (int i = 0; i < 2; ++i) {
                 const int b = c0 + 64 * half + lane + 32 * i;
                 if (b >= nblk) {
-                    if (SWZ && b < ncol_pad) srow[(b >> 2) * 512 + (b & 3)] = 0u;
+                    if (SWZ && b < ncol_pad) sf[sf_swizzled(r, b, nct)] = 0u;
                     continue;
                 }
                 uint2 c = make_uint2(0u, 0u);
@@ -720,7 +717,7 @@ __global__ void __launch_bounds__(256, 4) k_nvfp4_rht(const uint16_t* __restrict
                     sfb = bs.sf;
                 }
                 crow[b] = c;
-                srow[SWZ ? (b >> 2) * 512 + (b & 3) : b] = (uint8_t)sfb;
+                sf[SWZ ? sf_swizzled(r, b, nct) : r * nblk + b] = (uint8_t)sfb;
             }
         }
     }
