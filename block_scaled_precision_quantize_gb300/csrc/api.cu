@@ -454,7 +454,8 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
                  I32(L.row_src), cap, dev_status, stream);
     stage_mark(1, stream);
     launch_quant_scatter(static_cast<const uint16_t*>(x), T, H, (int32_t)topk, I32(L.slot_of), I32(L.offsets),
-                         I32(L.counts), (int32_t)E, ws + L.xq_codes, ws + L.xq_sf, F32(L.xq_scale), f46, sms, stream);
+                         I32(L.counts), (int32_t)E, ws + L.xq_codes, ws + L.xq_sf, F32(L.xq_scale), I32(L.row_src), cap, f46,
+                         sms, stream);
     if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_CUDA;
     stage_mark(2, stream);
 

@@ -78,7 +78,7 @@ void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_
                   cudaStream_t st);
 void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of,
                           const int32_t* offsets, const int32_t* counts, int32_t E, uint8_t* codes, uint8_t* sf,
-                          float* scale, bool four_six, int sms, cudaStream_t st);
+                          float* scale, int32_t* row_src, int64_t cap, bool four_six, int sms, cudaStream_t st);
 void launch_combine(const uint16_t* out, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of, const float* w,
                     uint16_t* y, int sms, cudaStream_t st);
 

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) k_route_hist(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ hist, int32_t* __restrict__ ticket,
                                                     int32_t* dev_status)
 {
+    pdl_enter();
     extern __shared__ int32_t sh[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(256) k_route_scan(int32_t* __restrict__ hist, 
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ ticket)
 {
+    pdl_enter();
     __shared__ int32_t warp_sums[8];
     __shared__ bool last;
     const int e = blockIdx.x;
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(256) k_route_assign_cta(const int32_t* __restr
                                                           const int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ slot_of, int32_t* __restrict__ row_src)
 {
+    pdl_enter();
     __shared__ int32_t fill[RT_CTA_MAX_E];
     __shared__ int32_t cnt[8][RT_CTA_MAX_E];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(32) k_route_assign(const int32_t* __restrict__
                                                      const int32_t* __restrict__ offsets,
                                                      int32_t* __restrict__ slot_of, int32_t* __restrict__ row_src)
 {
+    pdl_enter();
     extern __shared__ int32_t fill[];
     const int lane = threadIdx.x;
     for (int e = lane; e < E; e += 32) fill[e] = offsets[e] + hist[(int64_t)blockIdx.x * E + e];
@@ -192,7 +196,8 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ counts, int32_t E,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                       float* __restrict__ scale)
+                                                       float* __restrict__ scale, int32_t* __restrict__ row_src,
+                                                       int64_t cap)
 {
     const int TPC = (int)(blockDim.x >> 5) / WPR;  // tokens per CTA step (one per WPR warps)
     __shared__ uint32_t part_max[8];
@@ -202,14 +207,22 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
     const int64_t ncol_tiles = (nblk + 3) >> 2;
     // The padding rows of every expert segment (from its last routed row up to
     // the next 128-row boundary) get scale 0 and all-zero scale factors, so the
-    // GEMM's padding rows are exact zeros: one expert per CTA, one 4-byte
-    // scale-factor word per thread step.
-    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    // GEMM's padding rows are exact zeros, and row_src -1: one expert per CTA,
+    // one 4-byte scale-factor word per thread step.  The CTA after the last
+    // expert marks the capacity past the last segment (row_src -1).
+    for (int e = blockIdx.x; e <= E; e += gridDim.x) {
+        if (e == E) {
+            for (int64_t r = (int64_t)__ldg(offsets + E) + threadIdx.x; r < cap; r += blockDim.x) row_src[r] = -1;
+            continue;
+        }
         const int64_t p0 = (int64_t)__ldg(offsets + e) + __ldg(counts + e), p1 = __ldg(offsets + e + 1);
         for (int64_t i = threadIdx.x; i < (p1 - p0) * ncol_tiles; i += blockDim.x) {
             const int64_t r = p0 + i / ncol_tiles, wd = i % ncol_tiles;
             *reinterpret_cast<uint32_t*>(sf + sf_swizzled(r, 4 * wd, ncol_tiles)) = 0u;
-            if (wd == 0) scale[r] = 0.0f;
+            if (wd == 0) {
+                scale[r] = 0.0f;
+                row_src[r] = -1;
+            }
         }
     }
     // CTA-uniform loop (the shared-memory fold below synchronizes the CTA)
@@ -369,6 +382,22 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ ou
 }
 
 // ---------------------------------------------------------------------------
+template <typename... KArgs, typename... Args>
+static void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_t* hist, int32_t* counts,
                   int32_t* offsets, int32_t* slot_of, int32_t* row_src, int64_t capacity, int32_t* dev_status,
                   cudaStream_t st)
@@ -376,22 +405,27 @@ void launch_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E, int32_
     const int64_t n = T * topk;
     const int nchunks = (int)((n + RT_CHUNK - 1) / RT_CHUNK);
     int32_t* ticket = hist + (int64_t)std::max(nchunks, 1) * E;  // one word after the histograms
-    cudaMemsetAsync(row_src, 0xFF, (size_t)capacity * sizeof(int32_t), st);
+    (void)capacity;  // row_src of padding rows and unused capacity: k_quant_scatter
+    // the three phases with programmatic dependent launch: each starts while
+    // the previous one drains and waits for it (pdl_enter) before its loads
     if (nchunks > 0) {
-        k_route_hist<<<nchunks, 256, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, ticket, dev_status);
+        launch_pdl(k_route_hist, dim3(nchunks), dim3(256), (size_t)E * sizeof(int32_t), st, ids, n, E, hist, ticket,
+                   dev_status);
     } else {
         cudaMemsetAsync(ticket, 0, sizeof(int32_t), st);
     }
-    k_route_scan<<<E, 256, 0, st>>>(hist, nchunks, E, counts, offsets, ticket);
+    launch_pdl(k_route_scan, dim3(E), dim3(256), 0, st, hist, nchunks, E, counts, offsets, ticket);
     if (nchunks > 0 && E <= RT_CTA_MAX_E)
-        k_route_assign_cta<<<nchunks, 256, 0, st>>>(ids, n, E, hist, offsets, slot_of, row_src);
+        launch_pdl(k_route_assign_cta, dim3(nchunks), dim3(256), 0, st, ids, n, E, (const int32_t*)hist,
+                   (const int32_t*)offsets, slot_of, row_src);
     else if (nchunks > 0)
-        k_route_assign<<<nchunks, 32, (size_t)E * sizeof(int32_t), st>>>(ids, n, E, hist, offsets, slot_of, row_src);
+        launch_pdl(k_route_assign, dim3(nchunks), dim3(32), (size_t)E * sizeof(int32_t), st, ids, n, E,
+                   (const int32_t*)hist, (const int32_t*)offsets, slot_of, row_src);
 }
 
 void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk, const int32_t* slot_of,
                           const int32_t* offsets, const int32_t* counts, int32_t E, uint8_t* codes, uint8_t* sf,
-                          float* scale, bool four_six, int sms, cudaStream_t st)
+                          float* scale, int32_t* row_src, int64_t cap, bool four_six, int sms, cudaStream_t st)
 {
     const int nblk = (int)(H >> 4);
     // one warp per token in CTAs of 4 warps: at ~70 registers a thread, an SM
@@ -400,17 +434,17 @@ void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk,
 #define BSQ_QS(B)                                                                                                  \
     do {                                                                                                           \
         if (four_six)                                                                                              \
-            k_quant_scatter<B, true><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale); \
+            k_quant_scatter<B, true><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap); \
         else                                                                                                       \
-            k_quant_scatter<B, false><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale); \
+            k_quant_scatter<B, false><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap); \
     } while (0)
     if (nblk <= 32) BSQ_QS(1);
     else if (nblk <= 64) BSQ_QS(2);
     else if (nblk <= 128) BSQ_QS(4);
     else {  // wide rows: 4 warps per token, up to 4 blocks per lane (H <= 8192)
         const int grid4 = (int)std::max<int64_t>(1, std::min<int64_t>((T + 1) / 2, (int64_t)sms * 16));
-        if (four_six) k_quant_scatter<4, true, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);
-        else k_quant_scatter<4, false, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale);
+        if (four_six) k_quant_scatter<4, true, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap);
+        else k_quant_scatter<4, false, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap);
     }
 #undef BSQ_QS
 }
