@@ -492,7 +492,7 @@ bsq_status moe_expert_forward(const void* x, int64_t T, int64_t H, int64_t I, in
         if (launch_gemm_fp4(g1, stream) != cudaSuccess) return BSQ_ERR_CUDA;
         stage_mark(3, stream);
         launch_nvfp4_rows(reinterpret_cast<const uint16_t*>(ws + L.h), cap, I, I, ws + L.hq_codes, ws + L.hq_sf,
-                          F32(L.hq_scale), nullptr, 1, f46, true, sms, false, stream);
+                          F32(L.hq_scale), nullptr, 1, f46, true, sms, true, stream);
         stage_mark(4, stream);
     }
 

@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                                                        float* __restrict__ scale, int32_t* __restrict__ row_src,
                                                        int64_t cap)
 {
+    pdl_enter();
     const int TPC = (int)(blockDim.x >> 5) / WPR;  // tokens per CTA step (one per WPR warps)
     __shared__ uint32_t part_max[8];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ ou
                                                  int32_t topk, const int32_t* __restrict__ slot_of,
                                                  const float* __restrict__ w, uint16_t* __restrict__ y)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
@@ -434,17 +436,17 @@ void launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, int32_t topk,
 #define BSQ_QS(B)                                                                                                  \
     do {                                                                                                           \
         if (four_six)                                                                                              \
-            k_quant_scatter<B, true><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap); \
+            launch_pdl(k_quant_scatter<B, true>, dim3(grid), dim3(128), 0, st, x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap); \
         else                                                                                                       \
-            k_quant_scatter<B, false><<<grid, 128, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap); \
+            launch_pdl(k_quant_scatter<B, false>, dim3(grid), dim3(128), 0, st, x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap); \
     } while (0)
     if (nblk <= 32) BSQ_QS(1);
     else if (nblk <= 64) BSQ_QS(2);
     else if (nblk <= 128) BSQ_QS(4);
     else {  // wide rows: 4 warps per token, up to 4 blocks per lane (H <= 8192)
         const int grid4 = (int)std::max<int64_t>(1, std::min<int64_t>((T + 1) / 2, (int64_t)sms * 16));
-        if (four_six) k_quant_scatter<4, true, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap);
-        else k_quant_scatter<4, false, 4><<<grid4, 256, 0, st>>>(x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap);
+        if (four_six) launch_pdl(k_quant_scatter<4, true, 4>, dim3(grid4), dim3(256), 0, st, x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap);
+        else launch_pdl(k_quant_scatter<4, false, 4>, dim3(grid4), dim3(256), 0, st, x, T, H, topk, slot_of, offsets, counts, E, codes, sf, scale, row_src, cap);
     }
 #undef BSQ_QS
 }
@@ -453,7 +455,7 @@ void launch_combine(const uint16_t* out, int64_t T, int64_t H, int32_t topk, con
                     uint16_t* y, int sms, cudaStream_t st)
 {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 16));
-    k_combine<<<grid, 256, 0, st>>>(out, T, H, topk, slot_of, w, y);
+    launch_pdl(k_combine, dim3(grid), dim3(256), 0, st, out, T, H, topk, slot_of, w, y);
 }
 
 }  // namespace bsq

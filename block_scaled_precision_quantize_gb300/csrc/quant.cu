@@ -461,8 +461,8 @@ __global__ void k_philox_bits16(uint64_t seed, uint32_t stream, uint64_t idx0, i
 // launched while the previous one in the stream drains, and its kernel waits
 // for it in pdl_enter() before touching memory.  The standalone quantizer
 // entry points use it, so back-to-back calls overlap one call's tail with the
-// next one's launch; the MoE forward launches plainly (there the GEMM's
-// CTAs need the SMs to themselves).
+// next one's launch; in the MoE forward the light kernels use it and the
+// GEMMs launch plainly (their persistent CTAs need the SMs to themselves).
 template <typename... KArgs, typename... Args>
 static void launch_ks(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t st,
                       Args... args)
