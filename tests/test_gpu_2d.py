@@ -92,3 +92,17 @@ def test_2d_against_requantize_on_the_backward_workload():
     assert stats["2-D 16x16"][0] > 2 * stats["requant SR"][0]
     assert stats["2-D 16x16"][1] > stats["requant SR"][1]
     assert stats["1x16 of x^T"][1] <= stats["requant SR"][1]
+
+
+def test_2d_boundary_rows(O):
+    """Boundary rows (zeros, negative zeros, the bf16 maximum with both signs,
+    subnormals, E2M1 grid points, one non-zero, a huge dynamic range) in
+    16-row tiles: the tile maximum is taken on packed bf16 magnitudes."""
+    bsq = _bsq()
+    sp = synth.special_rows(96)
+    x = np.concatenate([np.repeat(sp, 2, axis=0), sp[::-1]]).astype(np.uint16)[:16 * (27 // 16 + 1)]
+    x = np.concatenate([x, np.zeros((32 - x.shape[0] % 32 if x.shape[0] % 32 else 0, 96), np.uint16)])
+    _check_against_oracle(O, x, bsq.quantize_nvfp4_2d(to_dev(x)))
+    # the tiles without the bf16 maximum (its tensor scale would flush them)
+    y = np.concatenate([sp[[0, 1, 4, 5, 6, 7, 8]]] * 3)[:16]
+    _check_against_oracle(O, y, bsq.quantize_nvfp4_2d(to_dev(y)))

@@ -171,6 +171,52 @@ def test_requant_page_example_on_gpu(gpu, O):
     assert abs(p3 - 0.25) < 0.005 and set(np.unique(nib[sel])) == {0x4, 0x5}
 
 
+def _requant_scale_edge_inputs():
+    """An NVFP4 input whose transposed rows exercise the block-scale quotient
+    amax / rn(6 t) at its edges.  Columns 0..15: row 0 sets every column
+    maximum to 2688 (E2M1 6 x E4M3 448 x t 1), so t = 1 and rn(6 t) = 6; in
+    the second, third and fourth 16-row blocks one row each holds E2M1 codes
+    c times scale s = 6.375, 6.375 (1 + 2^-22), 6.375 (1 - 2^-22): the
+    quotient is c * 1.0625 (exactly an E4M3 rounding midpoint for c = 0.5, 1,
+    2, 4: ties to even) or within 2^-20 of it.  Columns 16..31: one row with
+    t = 1e-38, so the column maximum is 6e-38 and 1 / rn(6 t) overflows."""
+    rows, K = 64, 32
+    codes = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    t = np.zeros(rows, np.float32)
+
+    def put(r, k, code):
+        b = int(codes[r, k // 2])
+        codes[r, k // 2] = (b & 0xF0) | code if k % 2 == 0 else (b & 0x0F) | (code << 4)
+
+    t[0], sf[0, 0] = 1.0, 0x7E
+    for k in range(16):
+        put(0, k, 0x7)
+    mags = [1, 2, 4, 6, 3, 5, 7, 0x9, 0xA, 0xC, 0xE]  # 0.5, 1, 2, 4 (ties), 1.5, 3, 6, negatives
+    for r, s in ((16, 6.375), (32, 6.375 * (1 + 2.0 ** -22)), (48, 6.375 * (1 - 2.0 ** -22))):
+        t[r], sf[r, 0] = np.float32(s), 0x38
+        for k in range(16):
+            put(r, k, mags[(k + r) % len(mags)])
+    t[1], sf[1, 1] = np.float32(1e-38), 0x38
+    for k in range(16, 32):
+        put(1, k, mags[k % len(mags)])
+    return codes, sf, t
+
+
+@pytest.mark.parametrize("sr", [False, True])
+@pytest.mark.parametrize("swz", [False, True])
+def test_requant_block_scale_quotient_edges(gpu, O, sr, swz):
+    codes, sf, t = _requant_scale_edge_inputs()
+    sf_in = O.sf_to_swizzled(sf) if swz else sf
+    out = gpu.requant_transpose_sr(to_dev(codes), to_dev(sf_in), to_dev(t), stochastic=sr, seed=5, swizzled=swz)
+    nc, ns, nt, mc, ms = O.requant_transpose(codes, sf, t, sr=sr, seed=5)
+    _check(to_np(out["nv_scale"]), nt, "nvfp4 scale")
+    _check(to_np(out["nv_sf"]), O.sf_to_swizzled(ns) if swz else ns, "nvfp4 sf")
+    _check(to_np(out["nv_codes"]), nc, "nvfp4 codes")
+    _check(to_np(out["mx_codes"]), mc, "mxfp8 codes")
+    _check(to_np(out["mx_sf"]), O.sf_to_swizzled(ms) if swz else ms, "mxfp8 sf")
+
+
 @pytest.mark.parametrize("shape", [(16384, 2048), (16384, 768)])
 def test_requant_full_size(gpu, O, shape):
     """The backward-requant workload at full size, SR seed 7, bit-exact."""

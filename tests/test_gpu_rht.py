@@ -69,3 +69,25 @@ def test_rht_on_the_outlier_workload():
     # the transform is orthogonal up to 32: its quantization error maps back with the same norm scale
     assert rel["rht"] < 0.5 and rel["plain"] < 0.5
     assert flush["rht"] < flush["plain"]
+
+
+def test_rht_boundary_rows(O):
+    """Boundary rows (zeros, negative zeros, bf16 subnormals, E2M1 grid points
+    and midpoints, one non-zero, a huge dynamic range; not the bf16 maximum,
+    whose 32-term sums overflow), a constant row and a row of repeated pairs,
+    whose butterfly sums cancel to exact zeros: the cross-lane stage's
+    fma(+-1, v, o) keeps the sign of every zero the separate add and subtract
+    give."""
+    bsq = _bsq()
+    sp = synth.special_rows(256)
+    keep = [0, 1, 4, 5, 6, 7, 8]
+    const = np.full((1, 256), synth.to_bf16_bits(np.array([1.5], np.float32))[0], np.uint16)
+    pairs = np.repeat(synth.normal((1, 128), seed=5), 2, axis=1)
+    x = np.concatenate([sp[keep], const, pairs]).astype(np.uint16)
+    for swizzled in (False, True):
+        c, s, t = bsq.quantize_nvfp4_rht(to_dev(x), seed=3, swizzled=swizzled)
+        rc, rs, rt = O.nvfp4_quantize_rht(x, seed=3)
+        assert first_mismatch(to_np(t).view(np.uint32), rt.view(np.uint32)) is None
+        assert first_mismatch(to_np(c), rc) is None, first_mismatch(to_np(c), rc)
+        want_sf = O.sf_to_swizzled(rs) if swizzled else rs
+        assert first_mismatch(to_np(s).reshape(want_sf.shape), want_sf) is None
