@@ -192,17 +192,18 @@ BSQ_DEVICE const uint8_t* sf_at(const uint8_t* sf, int64_t r, int64_t b, int64_t
 
 // ---------------------------------------------------------------------------
 // Column maxima of |D|, D = rn(rn(e2m1 * sf) * t).  Persistent: CTA (x, y)
-// of a grid of about two CTAs per SM owns the 512 columns of chunk x (lane l
-// the 16 columns of block 32 x + l: one 8-byte code load and one SF byte per
-// row) and, per warp, batches of 8 consecutive rows (batch y * 8 + warp, then
-// every 8 G-th, G = gridDim.y).  A batch's 24 loads are all in flight at once
-// and the next batch is loaded while the current one is folded (3-input max,
-// two rows per step); 8 rows from a multiple of 8 share one SF address
-// computation (in the swizzled layout they sit in one 32-row group, 16 bytes
-// apart).  The 8 warps' maxima are folded in shared memory and each column's
-// maximum goes to colmax with one unsigned atomicMax on the bits of a
-// non-negative float (order-independent, so deterministic).  colmax must hold
-// zeros beforehand.
+// of a grid of about four CTAs per SM (64 registers: 32 warps an SM to hide
+// the load latency) owns the 512 columns of chunk x (lane l the 16 columns of
+// block 32 x + l: one 8-byte code load and one SF byte per row) and, per
+// warp, batches of 8 consecutive rows (batch y * 8 + warp, then every 8 G-th,
+// G = gridDim.y).  A batch's 24 loads are all in flight at once, then folded
+// (3-input max, two rows per step); 8 rows from a multiple of 8 share one SF
+// address computation (in the swizzled layout they sit in one 32-row group,
+// 16 bytes apart).  Double-buffering the batches in registers (128 registers,
+// 2 CTAs an SM) was slower.  The 8 warps' maxima are folded in shared memory
+// and each column's maximum goes to colmax with one unsigned atomicMax on the
+// bits of a non-negative float (order-independent, so deterministic).  colmax
+// must hold zeros beforehand.
 constexpr int CM_COLS = 512;
 
 BSQ_DEVICE void cm_row(uint2 w, uint32_t sfb, float t, float (&d)[16])
@@ -218,7 +219,7 @@ BSQ_DEVICE void cm_row(uint2 w, uint32_t sfb, float t, float (&d)[16])
     }
 }
 
-struct CmBatch {
+struct CmBatch {  // one warp-batch of 8 rows: codes, SF bytes, row scales
     uint2 w[8];
     uint32_t s[8];
     float t[8];
@@ -255,7 +256,7 @@ BSQ_DEVICE void cm_fold(const CmBatch& B, float (&acc)[16])
 }
 
 template <bool SWZ>
-__global__ void __launch_bounds__(256, 2) k_rq_colmax(const uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(256, 4) k_rq_colmax(const uint8_t* __restrict__ codes,
                                                       const uint8_t* __restrict__ sf,
                                                       const float* __restrict__ row_scale, int64_t rows, int64_t K,
                                                       unsigned int* __restrict__ colmax)
@@ -270,17 +271,10 @@ __global__ void __launch_bounds__(256, 2) k_rq_colmax(const uint8_t* __restrict_
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
     if (b < nsf) {
-        CmBatch A, B;
-        int64_t bi = (int64_t)blockIdx.y * 8 + warp;
-        bool ha = cm_load<SWZ>(A, codes, sf, row_scale, bi, nbatch, b, nsf, ldc);
-        while (ha) {
-            const bool hb = cm_load<SWZ>(B, codes, sf, row_scale, bi + step, nbatch, b, nsf, ldc);
+        CmBatch A;
+        for (int64_t bi = (int64_t)blockIdx.y * 8 + warp; cm_load<SWZ>(A, codes, sf, row_scale, bi, nbatch, b, nsf, ldc);
+             bi += step)
             cm_fold(A, acc);
-            if (!hb) break;
-            ha = cm_load<SWZ>(A, codes, sf, row_scale, bi + 2 * step, nbatch, b, nsf, ldc);
-            cm_fold(B, acc);
-            bi += 2 * step;
-        }
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) red[warp][lane][j] = acc[j];
@@ -574,7 +568,7 @@ cudaError_t requant_passes(const uint8_t* codes, const uint8_t* sf, const float*
         int sms = 148;
         int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int64_t gy = std::max<int64_t>(1, std::min<int64_t>((2 * (int64_t)sms + chunks - 1) / chunks,
+        const int64_t gy = std::max<int64_t>(1, std::min<int64_t>((4 * (int64_t)sms + chunks - 1) / chunks,
                                                                   (rows / 8 + 7) / 8));
         const dim3 g1((unsigned)chunks, (unsigned)gy);
         if (swz) launch_pdl(k_rq_colmax<true>, g1, dim3(256), st, codes, sf, row_scale, rows, K, colmax);
