@@ -8,7 +8,6 @@
 // integer operations on bf16 magnitude bits and warp shuffles, and writes
 // packed codes with 8- to 32-byte stores.  Grids are sized in multiples of
 // the SM count.
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
