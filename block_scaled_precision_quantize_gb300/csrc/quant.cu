@@ -36,9 +36,11 @@ BSQ_DEVICE void store_sf(uint8_t* sf, bool swz, int64_t row, int64_t col, int64_
 // them) and reads them with 16-byte streaming loads.  TMODE 0: per-row scale
 // from the row maximum; TMODE 1: per-group scale from group_amax[row / rpg].
 // With SWZ the padding rows up to a multiple of 128 and the padding SF
-// columns are written as 0.
+// columns are written as 0.  The 4/6 form with swizzled scale factors and
+// four blocks a lane is held to 80 registers (3 CTAs of 256 threads an SM;
+// left free it takes 105 and an SM holds 16 warps instead of 24).
 template <int BPL, bool FOUR_SIX, bool SWZ, int TMODE, int LPR = 32>
-__global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+__global__ void __launch_bounds__(256, (FOUR_SIX && SWZ && BPL == 4) ? 3 : 0) k_nvfp4_rows(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                     int64_t ldx, uint8_t* __restrict__ codes,
                                                     uint8_t* __restrict__ sf, float* __restrict__ row_scale,
                                                     const float* __restrict__ group_amax, int64_t rpg)
@@ -109,9 +111,10 @@ __global__ void __launch_bounds__(256) k_nvfp4_rows(const uint16_t* __restrict__
 // lane (one warp per row would need 8-16 blocks per lane, i.e. more registers
 // and so fewer warps in flight).  A CTA of 8 warps takes 2 rows per step; the
 // row maximum is folded across the row's warps in shared memory.  Lane l of
-// part p owns blocks 32 p + l + 128 i.
+// part p owns blocks 32 p + l + 128 i.  The 4/6 form with swizzled scale
+// factors is held to 80 registers, as in k_nvfp4_rows.
 template <bool FOUR_SIX, bool SWZ, int TMODE>
-__global__ void __launch_bounds__(256) k_nvfp4_rows_wide(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+__global__ void __launch_bounds__(256, (FOUR_SIX && SWZ) ? 3 : 0) k_nvfp4_rows_wide(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                          int64_t ldx, uint8_t* __restrict__ codes,
                                                          uint8_t* __restrict__ sf, float* __restrict__ row_scale,
                                                          const float* __restrict__ group_amax, int64_t rpg)
