@@ -12,9 +12,11 @@ rank runs its own replica: weak scaling, no collective on the data path).
 The working set (~0.9 GB: weights, activations, workspace) is larger than the
 129 MB L2, so no flush is needed between steps.
 
-Also reported: per-stage times (CUDA events recorded by the library on the
-launching stream inside the timed region), a roofline for the dominant
-kernel, the standalone quantizers (MXFP8 row+col on 16384x2048, NVFP4
+Also reported: per-stage times (CUDA events the library records at the
+stage boundaries on the launching stream, from a second pass right after the
+timed one), each data-moving stage's HBM floor (its bytes at the measured copy
+rate, or its written bytes at the write-only rate measured in the same run,
+whichever takes longer), a roofline for the dominant kernel, the standalone quantizers (MXFP8 row+col on 16384x2048, NVFP4
 per-token on 16384x2048, requant with Philox SR and round-to-nearest on
 16384x2048 and 16384x768; back-to-back launches through the C ABI rotating
 over input/output sets larger than twice the L2, so every launch starts
@@ -117,6 +119,71 @@ def measure_mma_ceiling(bsq, dev, P, iters=4096, reps=10):
     P["fp4_source"] = "measured in this run: back-to-back tcgen05.mma kind::mxf4nvf4 (bsq_mma_ceiling), best form"
     P["fp8_source"] = "measured in this run: back-to-back tcgen05.mma kind::mxf8f6f4 (bsq_mma_ceiling), best form"
     return out
+
+
+def measure_write_bw(dev, P, nbytes=1 << 31, reps=5):
+    """HBM write-only rate of this GPU: a fill of a 2 GiB buffer (torch's
+    fill kernel; bytes written / CUDA-event time, best of `reps`).  Stored
+    in P as the denominator of the write side of a stage's HBM floor."""
+    import torch
+    buf = torch.empty(nbytes // 4, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        buf.fill_(1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+    torch.cuda.synchronize()
+    for r in range(reps):
+        ev[2 * r].record()
+        buf.fill_(r)
+        ev[2 * r + 1].record()
+    torch.cuda.synchronize()
+    ms = min(ev[2 * r].elapsed_time(ev[2 * r + 1]) for r in range(reps))
+    del buf
+    P["hbm_write_gbs"] = nbytes / (ms * 1e-3) / 1e9
+    P["hbm_write_source"] = "measured in this run: fill of a 2 GiB buffer, bytes written / time, best of 5"
+    return P["hbm_write_gbs"]
+
+
+STAGES = ["route", "quantize_scatter", "gemm1_swiglu", "quantize_h", "gemm2", "combine"]
+
+
+def stage_traffic(w, R_pad):
+    """Algorithmic HBM bytes (read, written) of the forward's stages that
+    move data: x read once and each routed copy of its codes, scale factors
+    and token scale written; h read and quantized; GEMM2's A, weights and
+    bf16 per-slot outputs; the per-slot outputs gathered and y written."""
+    T, H, I, E, k = w["T"], w["H"], w["I"], w["E"], w["k"]
+    R = T * k
+    return {"quantize_scatter": (T * H * 2, R * (H // 2 + H // 16 + 4)),
+            "quantize_h": (R_pad * I * 2, R_pad * (I // 2 + I // 16 + 4)),
+            "gemm2": (R_pad * (I // 2 + I // 16 + 4) + E * H * (I // 2 + I // 16), R_pad * H * 2),
+            "combine": (R * H * 2 + R * 8, T * H * 2)}
+
+
+def stage_table(ev, w, R_pad, P):
+    """Mean stage times over the event rows `ev`, with each stage's rate:
+    TFLOP/s for the GEMMs; for the stages that move data, GB/s against the
+    measured copy rate, and the HBM floor, the longer of (all bytes at the
+    copy rate) and (the bytes written at the write-only rate)."""
+    f1, f2 = gemm_flops(w)
+    traffic = stage_traffic(w, R_pad)
+    stages = {}
+    for s, n in enumerate(STAGES):
+        ms = statistics.mean(row[s].elapsed_time(row[s + 1]) for row in ev)
+        d = {"ms": ms}
+        if n in ("gemm1_swiglu", "gemm2"):
+            d["tflops"] = (f1 if n == "gemm1_swiglu" else f2) / (ms * 1e-3) / 1e12
+            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops"]
+        if n in traffic:
+            rd, wr = traffic[n]
+            if n != "gemm2":
+                d["gbs"] = (rd + wr) / (ms * 1e-3) / 1e9
+                d["frac_of_hbm"] = d["gbs"] / P["hbm_gbs"]
+            if "hbm_write_gbs" in P:
+                floor = max((rd + wr) / (P["hbm_gbs"] * 1e9), wr / (P["hbm_write_gbs"] * 1e9)) * 1e3
+                d["hbm_floor_ms"] = floor
+                d["frac_of_hbm_floor"] = floor / ms
+        stages[n] = d
+    return stages
 
 
 # ----------------------------------------------------------------- clocks
@@ -503,13 +570,11 @@ def run_ours(args, w, rank, world, local):
         fwd()
     bsq.set_stage_events(None)
     torch.cuda.synchronize()
-    # the roofline's tensor denominators, measured under the same clock sampling
+    # the roofline's tensor denominators and the write-only HBM rate,
+    # measured under the same clock sampling
     ceiling = measure_mma_ceiling(bsq, dev, P)
+    measure_write_bw(dev, P)
     clk = clocks.stop()
-
-    names = ["route", "quantize_scatter", "gemm1_swiglu", "quantize_h", "gemm2", "combine"]
-    stage_ms = {n: statistics.mean(stage_ev[i][s].elapsed_time(stage_ev[i][s + 1]) for i in range(Ks))
-                for s, n in enumerate(names)}
     # the same step with h quantized inside GEMM1's epilogue (moe_expert_forward
     # with BSQ_MOE_FUSED_H: bit-identical results), timed for comparison
     fe0, fe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -532,27 +597,11 @@ def run_ours(args, w, rank, world, local):
     offsets = torch.empty(E + 1, dtype=torch.int32)
     offsets.copy_(ws[L.offsets:L.offsets + 4 * (E + 1)].view(torch.int32))
     R_pad = int(offsets[-1])
-    stage_bytes = {
-        "quantize_scatter": T * H * 2 + R * (H // 2 + H // 16 + 4),
-        "quantize_h": R_pad * I * 2 + R_pad * (I // 2 + I // 16 + 4),
-        "combine": R * H * 2 + T * H * 2 + R * 8,
-    }
-    stages = {}
-    for n in names:
-        d = {"ms": stage_ms[n]}
-        if n == "gemm1_swiglu":
-            d.update(tflops=f1 / (stage_ms[n] * 1e-3) / 1e12)
-            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops"]
-        elif n == "gemm2":
-            d.update(tflops=f2 / (stage_ms[n] * 1e-3) / 1e12)
-            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops"]
-        elif n in stage_bytes:
-            d.update(gbs=stage_bytes[n] / (stage_ms[n] * 1e-3) / 1e9)
-            d["frac_of_hbm"] = d["gbs"] / P["hbm_gbs"]
-        stages[n] = d
+    stages = stage_table(stage_ev, w, R_pad, P)
+    stage_ms = {n: d["ms"] for n, d in stages.items()}
 
     # roofline of the dominant kernel
-    dom = max(names, key=lambda n: stage_ms[n])
+    dom = max(STAGES, key=lambda n: stage_ms[n])
     gemm_hash = source_hash("gemm_fp4.cu", "common.cuh", "tc_ptx.cuh")
     if dom in ("gemm1_swiglu", "gemm2"):
         fl = f1 if dom == "gemm1_swiglu" else f2
@@ -564,7 +613,7 @@ def run_ours(args, w, rank, world, local):
                 "frac_of_bf16_burst_x6": ach / (P["bf16_tflops"] * 6.0),
                 "frac_of_page_15pf": ach / 15000.0}
     else:
-        ach = stage_bytes.get(dom, 0) / (stage_ms[dom] * 1e-3) / 1e9
+        ach = stages[dom].get("gbs", 0.0)
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / P["hbm_gbs"], "traffic": None, "peak_source": P["source"]}
 
@@ -645,7 +694,8 @@ def run_ours(args, w, rank, world, local):
                        "gemm_tflop_per_step": flops / 1e12,
                        "l2": "working set ~1 GB > 129 MB L2; no flush between steps; components rotate input sets > 2x L2",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roof, "mma_ceiling": ceiling, "stages": stages, "components": components, "e2e": e2e,
+            "roofline": roof, "mma_ceiling": ceiling,
+            "hbm_write": {"gbs": P["hbm_write_gbs"], "source": P["hbm_write_source"]}, "stages": stages, "components": components, "e2e": e2e,
             "step_with_h_quantized_in_gemm1_ms": fused_h_ms, "second_record": second,
             "gpu_launches": KERNELS_PER_STEP * K, "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -699,26 +749,11 @@ def layer_record(bsq, synth, w, dev, P, steps=10, warmup=3):
     bsq.set_stage_events(None)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    names = ["route", "quantize_scatter", "gemm1_swiglu", "quantize_h", "gemm2", "combine"]
-    stage_ms = {n: statistics.mean(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(steps))
-                for s, n in enumerate(names)}
     f1, f2 = gemm_flops(w)
     R = T * k
     L = bsq.moe_workspace_layout(T, H, I, E, k)
     R_pad = int(ws[L.offsets + 4 * E:L.offsets + 4 * (E + 1)].view(torch.int32).item())
-    stage_bytes = {"quantize_scatter": T * H * 2 + R * (H // 2 + H // 16 + 4),
-                   "quantize_h": R_pad * I * 2 + R_pad * (I // 2 + I // 16 + 4),
-                   "combine": R * H * 2 + T * H * 2 + R * 8}
-    stages = {}
-    for n in names:
-        d = {"ms": stage_ms[n]}
-        if n in ("gemm1_swiglu", "gemm2"):
-            d["tflops"] = (f1 if n == "gemm1_swiglu" else f2) / (stage_ms[n] * 1e-3) / 1e12
-            d["frac_of_fp4_peak"] = d["tflops"] / P["fp4_tflops"]
-        elif n in stage_bytes:
-            d["gbs"] = stage_bytes[n] / (stage_ms[n] * 1e-3) / 1e9
-            d["frac_of_hbm"] = d["gbs"] / P["hbm_gbs"]
-        stages[n] = d
+    stages = stage_table(ev, w, R_pad, P)
     del x, ids_d, wts_d, wgu, wd, ws, y
     torch.cuda.empty_cache()
     return {"workload": w["name"], "metric": METRIC, "value": (f1 + f2) / (ms_step * 1e-3) / 1e12,
