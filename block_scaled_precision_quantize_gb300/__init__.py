@@ -23,6 +23,7 @@ __all__ = [
     "grouped_expert_gemm_fp4", "grouped_expert_gemm_mxfp8", "moe_expert_forward",
     "moe_workspace_layout", "moe_workspace_size", "requant_workspace_size",
     "sf_swizzle", "sf_unswizzle", "format_probe", "philox_bits16", "sf_swizzled_bytes", "mma_ceiling",
+    "check_status",
     "SF_SWIZZLED", "FOUR_SIX", "STOCHASTIC", "MOE_FUSED_H", "MOE_KEEP_H", "EPI_F32", "EPI_BF16", "EPI_SWIGLU_BF16",
 ]
 
@@ -57,6 +58,7 @@ class MoeLayout(ctypes.Structure):
 _SIGS = {
     "bsq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bsq_version": (_I32, []),
+    "bsq_check_status": (ctypes.c_int, [_P, ctypes.POINTER(_I32), _P]),
     "quantize_nvfp4_per_token": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P, _P]),
     "quantize_nvfp4_per_expert": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P, _P]),
     "quantize_mxfp8_rowcol": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _U32, _P, _P]),
@@ -138,6 +140,17 @@ def _ptr(t):
 
 def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def check_status(dev_status) -> int:
+    """The device status word `dev_status` (int32 CUDA tensor) read back on
+    the current stream after the work enqueued there (bsq_check_status:
+    waits for the stream).  Returns DEV_OK or the first DEV_* recorded."""
+    _cuda(dev_status, "dev_status")
+    out = _I32(0)
+    _check(load().bsq_check_status(_ptr(dev_status), ctypes.byref(out), _stream(dev_status.device)),
+           "bsq_check_status")
+    return int(out.value)
 
 
 def _cuda(t, name):

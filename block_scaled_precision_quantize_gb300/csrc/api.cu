@@ -85,6 +85,17 @@ const char* bsq_status_string(bsq_status s)
 
 int32_t bsq_version(void) { return 100; }
 
+bsq_status bsq_check_status(const int32_t* dev_status, int32_t* status, bsq_stream_t stream)
+{
+    if (!dev_status || !status) return BSQ_ERR_NULL;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return BSQ_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return BSQ_ERR_CUDA;
+    *status = v;
+    return BSQ_OK;
+}
+
 bsq_status bsq_set_stage_events(void* const* events, int32_t n)
 {
     if (events && n < 7) return BSQ_ERR_SHAPE;

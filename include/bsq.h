@@ -92,6 +92,16 @@ typedef enum {
 const char* bsq_status_string(bsq_status s);
 int32_t bsq_version(void);
 
+/* bsq_check_status: reads a dev_status word back to the host.  It copies the
+ * device int32 at dev_status into *status on `stream`, after the work already
+ * enqueued there, and waits for the stream.  This is the one call of the
+ * library that synchronizes.  *status gets BSQ_DEV_OK or the first
+ * BSQ_DEV_* value a kernel recorded; the word itself is left as it is, so
+ * the caller zeroes it before reusing it.  Returns BSQ_ERR_NULL if either
+ * pointer is NULL and BSQ_ERR_CUDA if the copy or the wait fails (an earlier
+ * asynchronous CUDA error of the stream included). */
+bsq_status bsq_check_status(const int32_t* dev_status, int32_t* status, bsq_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * quantize_nvfp4_per_token: per-row (per-token) NVFP4 quantization.
  * "4ビットの教訓" (hackernews.jp), "ベースラインレシピ": each token computes its

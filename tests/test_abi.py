@@ -43,6 +43,10 @@ def test_host_validation_without_a_gpu(lib):
     import block_scaled_precision_quantize_gb300 as bsq
     P = ctypes.c_void_p
     dummy = P(4096)
+    word = ctypes.c_int32(-1)
+    assert lib.bsq_check_status(None, ctypes.byref(word), None) == 1  # null status word
+    assert lib.bsq_check_status(dummy, None, None) == 1               # null destination
+    assert word.value == -1                                            # nothing written
     st = lib.quantize_nvfp4_per_token(dummy, 8, 256, 256, dummy, dummy, dummy, 1 << 7, None, None)
     assert st == 4  # flags
     st = lib.quantize_nvfp4_per_token(dummy, 8, 250, 256, dummy, dummy, dummy, 0, None, None)

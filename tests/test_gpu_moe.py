@@ -169,9 +169,15 @@ def test_moe_bad_expert_id_reported(gpu):
     wd = gpu.quantize_nvfp4_per_expert(to_dev(synth.normal((E, H, I), seed=3, std=0.02)))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, dev_status=status)
+    # bsq_check_status reads the word after the stream's work, and leaves it
+    assert gpu.check_status(status) == gpu.DEV_BAD_EXPERT
     torch.cuda.synchronize()
     assert int(status.item()) == gpu.DEV_BAD_EXPERT
     assert torch.isfinite(y.float()).all()
+    ids[5, 1] = 2
+    status.zero_()
+    gpu.moe_expert_forward(to_dev(x), to_dev(ids), to_dev(wts), wgu, wd, I, dev_status=status)
+    assert gpu.check_status(status) == gpu.DEV_OK
 
 
 def test_moe_qwen3_shaped_sampled(gpu, O):
