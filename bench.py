@@ -123,8 +123,10 @@ def measure_mma_ceiling(bsq, dev, P, iters=4096, reps=10):
 
 def measure_write_bw(dev, P, nbytes=1 << 31, reps=5):
     """HBM write-only rate of this GPU: a fill of a 2 GiB buffer (torch's
-    fill kernel; bytes written / CUDA-event time, best of `reps`).  Stored
-    in P as the denominator of the write side of a stage's HBM floor."""
+    fill kernel, one value throughout; bytes written / CUDA-event time, best
+    of `reps`).  Stored in P as the denominator of the write side of a
+    stage's HBM floor; data that varies may write more slowly, so the floor
+    it gives is a lower bound on the time."""
     import torch
     buf = torch.empty(nbytes // 4, dtype=torch.int32, device=dev)
     for _ in range(2):
